@@ -1,0 +1,352 @@
+"""The indexer decode path, stated plainly (test infrastructure).
+
+Slow, exact CPU statement of each step, following the pages:
+
+* NVFP4 page fields and dequantisation - "vllm.models.minimax_m3.nvidia.ops.
+  gather_nvfp4_index_k", module docstring and the
+  ``minimax_m3_gather_nvfp4_index_k_fp8`` parameter list.
+* Decode scoring contract (eight query slots, pages below a query's own page)
+  - "vllm.models.minimax_m3.nvidia.indexer_nvfp4_decode_cp", module docstring;
+  own page and width clamp - its ``_local_topk_push_kernel``; page count -
+  its ``_compact_block_table_kernel``.
+* Page keys - the same page's ``_page_keys``; key order and special values -
+  "wolfcomos/MSA PR #1", sections "Changes" and "Behaviour changes".
+* Row assembly (short rows, 15 ranked pages then the own page) - the
+  ``_merge_kernel`` of the decode-CP page.
+* Multi-token scorer - "Mojo module sparse_index_fp8_sm100", module text.
+
+Readings where the pages leave a step open (listed again in the design
+notes): the page reduction is the max over the page's 128 keys of
+q_scale * (q . k) in fp32 (the dot rounded once to fp32, then one fp32
+multiply); page bytes are all 8,192 code bytes, then the 1,024 scale bytes
+at 8192 + token * 8 + group, group = element // 16; a NaN scale dequantises
+to 0x7F; the page field of a key is 32 bits wide; a page whose block id is
+out of range scores NaN (ranked as -inf) and raises a status bit.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from .formats import E2M1_VALUES, E4M3_VALUES, e4m3_encode
+
+PAGE_TOKENS = 128
+HEAD_DIM = 128
+CODE_BYTES = PAGE_TOKENS * HEAD_DIM // 2  # 8192
+PAGE_BYTES = CODE_BYTES + PAGE_TOKENS * HEAD_DIM // 16  # 9216
+SLOTS = 8
+INDEX_HEADS = 4
+ROWS = SLOTS * INDEX_HEADS  # 32 score rows per request, row = slot * 4 + head
+TOPK = 16
+RANKED = 15  # pages ranked by key before the own page is appended
+
+# device status bits (same meaning as the library's)
+ST_BLOCK_OOR = 1  # a block id outside [0, num_blocks): page skipped
+ST_LEN_CLAMPED = 2  # a request held more pages than the table / buffer: clamped
+ST_BAD_OUTPUT = 4  # an output page index outside the output buffer: skipped
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 pages
+# ---------------------------------------------------------------------------
+
+def page_fields(page: np.ndarray):
+    """Split one packed page into E2M1 codes [128, 128] and E4M3 scales [128, 8].
+
+    Token t's 64 code bytes start at t * 64; element d sits in byte
+    t * 64 + d // 2, low nibble for even d, high nibble for odd d.  The
+    scales follow all codes: scale (t, g) at byte 8192 + t * 8 + g.
+    """
+    flat = np.asarray(page, dtype=np.uint8).reshape(PAGE_BYTES)
+    code_bytes = flat[:CODE_BYTES].reshape(PAGE_TOKENS, HEAD_DIM // 2)
+    codes = np.empty((PAGE_TOKENS, HEAD_DIM), dtype=np.uint8)
+    codes[:, 0::2] = code_bytes & 0x0F
+    codes[:, 1::2] = code_bytes >> 4
+    scales = flat[CODE_BYTES:].reshape(PAGE_TOKENS, HEAD_DIM // 16)
+    return codes, scales
+
+
+def dequant_page(page: np.ndarray) -> np.ndarray:
+    """[128, 128] E4M3 bytes: e4m3_rn_satfinite(e2m1(code) * e4m3(scale)).
+
+    The product of an E2M1 value (at most 2 significant bits) and an E4M3
+    value (at most 4) is exact in float64; ``e4m3_encode`` rounds it once.
+    """
+    codes, scales = page_fields(page)
+    group_scale = scales[:, np.arange(HEAD_DIM) // 16]
+    x = E2M1_VALUES[codes] * E4M3_VALUES[group_scale]
+    return e4m3_encode(x)
+
+
+def gather_dequant(kv, bt, num_pages, page_offsets, max_num_pages, out_pages, out=None):
+    """Gather each request's first num_pages[r] logical pages and dequantise.
+
+    Mirrors ``minimax_m3_gather_nvfp4_index_k_fp8``: request r's logical page
+    p < min(num_pages[r], max_num_pages) (and < the table's width) is
+    physical page bt[r, p], written at output page page_offsets[r] + p.
+    Pages with an out-of-range block id or output index are skipped and
+    flagged.  Returns (out, status).
+    """
+    kv = np.asarray(kv).reshape(-1, PAGE_BYTES)
+    num_blocks = kv.shape[0]
+    bt = np.asarray(bt)
+    if out is None:
+        out = np.zeros((out_pages, PAGE_TOKENS, HEAD_DIM), dtype=np.uint8)
+    status = 0
+    for r in range(bt.shape[0]):
+        n = min(int(num_pages[r]), int(max_num_pages), bt.shape[1])
+        for p in range(max(n, 0)):
+            blk = int(bt[r, p])
+            dst = int(page_offsets[r]) + p
+            if not (0 <= blk < num_blocks):
+                status |= ST_BLOCK_OOR
+                continue
+            if not (0 <= dst < out_pages):
+                status |= ST_BAD_OUTPUT
+                continue
+            out[dst] = dequant_page(kv[blk])
+    return out, status
+
+
+# ---------------------------------------------------------------------------
+# decode scores
+# ---------------------------------------------------------------------------
+
+def e4m3_units(b: np.ndarray) -> np.ndarray:
+    """E4M3 bytes -> exact int64 multiples of 2^-9 (every finite E4M3 value is one)."""
+    v = E4M3_VALUES[np.asarray(b, dtype=np.uint8)]
+    if np.isnan(v).any():
+        raise ValueError("oracle scores need finite E4M3 inputs")
+    return np.rint(v * 512.0).astype(np.int64)
+
+
+def page_scores(q_rows: np.ndarray, q_scale: np.ndarray, kdeq: np.ndarray) -> np.ndarray:
+    """Score of one page for each query row: max over the 128 keys of
+    fp32(q_scale * fp32(q . k)).
+
+    q_rows [R, 128] E4M3 bytes, q_scale [R] float32, kdeq [128, 128] E4M3
+    bytes (token, depth).  The dot is exact in int64 (units of 2^-18), then
+    rounded once to fp32 and multiplied by q_scale in fp32.
+    """
+    qi = e4m3_units(q_rows)
+    ki = e4m3_units(kdeq)
+    dot = qi @ ki.T  # [R, 128 keys], exact
+    d32 = (dot.astype(np.float64) * 2.0 ** -18).astype(np.float32)
+    v = d32 * np.asarray(q_scale, dtype=np.float32)[:, None]
+    return v.max(axis=1)
+
+
+def page_score_bound(q_rows: np.ndarray, q_scale: np.ndarray, kdeq: np.ndarray) -> np.ndarray:
+    """Per-row tolerance 1e-3 * max_t sum_d |q_scale * q_d * k_td| (float64)."""
+    qi = np.abs(e4m3_units(q_rows)).astype(np.float64)
+    ki = np.abs(e4m3_units(kdeq)).astype(np.float64)
+    mag = (qi @ ki.T) * 2.0 ** -18 * np.abs(np.asarray(q_scale, dtype=np.float64))[:, None]
+    return 1e-3 * mag.max(axis=1)
+
+
+def own_page(seq_len: int, query_len: int, i: int) -> int:
+    """Own page of query i (slot 8 - query_len + i): (seq_len - query_len + i) // 128, floored."""
+    return (int(seq_len) - int(query_len) + int(i)) // PAGE_TOKENS
+
+
+def scored_pages(seq_len: int, max_blocks: int, width: int) -> int:
+    """Pages scored for a request: (seq_len - 1) // 128, clamped to [0, min(table, width)]."""
+    hist = (int(seq_len) - 1) // PAGE_TOKENS
+    return max(0, min(hist, int(max_blocks), int(width)))
+
+
+def decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, pages=None):
+    """Scores [B, 32, width] float32 of every (slot, head) row for the pages below
+    the slot's own page; untouched entries stay NaN.
+
+    Returns (scores, written mask, bound, status).  ``pages`` optionally
+    restricts the work to a list of (b, j) pairs (sampled checks).
+    """
+    kv = np.asarray(kv).reshape(-1, PAGE_BYTES)
+    num_blocks = kv.shape[0]
+    B = len(seq_lens)
+    scores = np.full((B, ROWS, width), np.nan, dtype=np.float32)
+    written = np.zeros((B, ROWS, width), dtype=bool)
+    bound = np.zeros((B, ROWS, width), dtype=np.float64)
+    status = 0
+    if pages is None:
+        pages = [(b, j) for b in range(B) for j in range(scored_pages(seq_lens[b], max_blocks, width))]
+    for b in range(B):
+        if (int(seq_lens[b]) - 1) // PAGE_TOKENS > min(int(max_blocks), int(width)):
+            status |= ST_LEN_CLAMPED
+    for b, j in pages:
+        if j >= scored_pages(seq_lens[b], max_blocks, width):
+            continue
+        blk = int(bt[b, j])
+        q_rows = np.asarray(q[b]).reshape(ROWS, HEAD_DIM)
+        qs = np.asarray(q_scale[b]).reshape(ROWS)
+        if 0 <= blk < num_blocks:
+            kdeq = dequant_page(kv[blk])
+            s = page_scores(q_rows, qs, kdeq)
+            bd = page_score_bound(q_rows, qs, kdeq)
+        else:
+            status |= ST_BLOCK_OOR
+            s = np.full(ROWS, np.nan, dtype=np.float32)
+            bd = np.zeros(ROWS)
+        for i in range(query_len):
+            slot = SLOTS - query_len + i
+            if j < own_page(seq_lens[b], query_len, i):
+                rows = slice(slot * INDEX_HEADS, (slot + 1) * INDEX_HEADS)
+                scores[b, rows, j] = s[rows]
+                written[b, rows, j] = True
+                bound[b, rows, j] = bd[rows]
+    return scores, written, bound, status
+
+
+# ---------------------------------------------------------------------------
+# keys and exact top-16
+# ---------------------------------------------------------------------------
+
+def canonical_scores(x: np.ndarray, forced: np.ndarray) -> np.ndarray:
+    """Forced pages rank as +inf, NaN as -inf, -0 as +0."""
+    x = np.asarray(x, dtype=np.float32).copy()
+    x[np.isnan(x)] = -np.inf
+    x[x == 0] = np.float32(0.0)
+    x[forced] = np.inf
+    return x
+
+
+def page_keys(x: np.ndarray, cols: np.ndarray, forced: np.ndarray) -> np.ndarray:
+    """64-bit keys: order-preserving score bits above the inverted column.
+
+    ordered = bits ^ (sign ? 0xFFFFFFFF : 0x80000000) maps fp32 order onto
+    unsigned order; key = ordered << 32 | (0xFFFFFFFF - col), so keys are
+    distinct and sort by score descending, then column ascending.
+    """
+    bits = canonical_scores(x, forced).view(np.uint32).astype(np.uint64)
+    neg = (bits >> np.uint64(31)) != 0
+    ordered = np.where(neg, bits ^ np.uint64(0xFFFFFFFF), bits ^ np.uint64(0x80000000))
+    return (ordered << np.uint64(32)) | (np.uint64(0xFFFFFFFF) - np.asarray(cols, dtype=np.uint64))
+
+
+def key_column(keys: np.ndarray) -> np.ndarray:
+    keys = np.asarray(keys, dtype=np.uint64)
+    col = (np.uint64(0xFFFFFFFF) - (keys & np.uint64(0xFFFFFFFF))).astype(np.int64)
+    return np.where(keys == 0, -1, col).astype(np.int32)
+
+
+def top16(row: np.ndarray, n: int, force_begin: int = 0, force_end: int = 0):
+    """Exact top-16 columns of row[:n] by key, descending; -1 / key 0 pad.
+
+    Columns in [force_begin, force_end) rank as +inf.  n is clamped to the
+    row's width ("a length past the page table ranks what it holds").
+    """
+    row = np.asarray(row, dtype=np.float32)
+    n = max(0, min(int(n), row.shape[0]))
+    cols = np.arange(n)
+    forced = (cols >= force_begin) & (cols < force_end)
+    keys = np.sort(page_keys(row[:n], cols, forced))[::-1][:TOPK]
+    out_keys = np.zeros(TOPK, dtype=np.uint64)
+    out_keys[: len(keys)] = keys
+    return key_column(out_keys), out_keys
+
+
+def topk16_select(scores: np.ndarray, valid_n=None, force_begin: int = 0, force_end: int = 0):
+    """top16 of every row of a [rows, width] fp32 matrix."""
+    scores = np.asarray(scores, dtype=np.float32)
+    rows, width = scores.shape
+    idx = np.full((rows, TOPK), -1, dtype=np.int32)
+    keys = np.zeros((rows, TOPK), dtype=np.uint64)
+    for r in range(rows):
+        n = width if valid_n is None else int(valid_n[r])
+        idx[r], keys[r] = top16(scores[r], n, force_begin, force_end)
+    return idx, keys
+
+
+def decode_row(own: int, scores_row: np.ndarray, n_scored: int) -> np.ndarray:
+    """One output row of the decode step.
+
+    own + 1 <= 16: pages 0..own, then -1.  Otherwise the 15 best pages
+    below own (among those scored), then own.
+    """
+    k = np.arange(TOPK)
+    if own + 1 <= TOPK:
+        return np.where(k <= own, k, -1).astype(np.int32)
+    idx, _ = top16(scores_row, min(own, n_scored))
+    out = idx.copy()
+    out[RANKED] = own
+    return out.astype(np.int32)
+
+
+def decode_step(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, scores=None):
+    """Indexer decode step: out [B, query_len, 4, 16] int32.
+
+    ``scores`` lets a test rank a given score buffer (for instance the GPU's
+    own) instead of the oracle's, which checks the selection bit for bit.
+    Returns (out, scores, status).
+    """
+    status = 0
+    if scores is None:
+        scores, _, _, status = decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks)
+    B = len(seq_lens)
+    out = np.full((B, query_len, INDEX_HEADS, TOPK), -1, dtype=np.int32)
+    for b in range(B):
+        n = scored_pages(seq_lens[b], max_blocks, width)
+        for i in range(query_len):
+            slot = SLOTS - query_len + i
+            own = own_page(seq_lens[b], query_len, i)
+            for h in range(INDEX_HEADS):
+                out[b, i, h] = decode_row(own, scores[b, slot * INDEX_HEADS + h], n)
+    return out, scores, status
+
+
+# ---------------------------------------------------------------------------
+# multi-token relu-weighted scorer
+# ---------------------------------------------------------------------------
+
+def mtp_token_scores(q_tok, q_scale_tok, k_keys, k_scale_keys):
+    """score[key] = k_scale[key] * sum_h relu(q[h] . k[key]) * q_scale[h].
+
+    q_tok [H, 128] E4M3 bytes, q_scale_tok [H] f32, k_keys [N, 128] E4M3
+    bytes, k_scale_keys [N] f32.  Dots exact in int64, relu written as
+    (x + |x|) / 2, products and the head sum in float64, one rounding to fp32.
+    Returns (scores f32 [N], bound f64 [N]) with bound = 1e-3 * k_scale *
+    sum_h |q_scale_h| sum_d |q_hd k_d|.
+    """
+    qi = e4m3_units(q_tok)
+    ki = e4m3_units(k_keys)
+    dots = (qi @ ki.T).astype(np.float64) * 2.0 ** -18  # [H, N]
+    relu = (dots + np.abs(dots)) * 0.5
+    qs = np.asarray(q_scale_tok, dtype=np.float64)[:, None]
+    ks = np.asarray(k_scale_keys, dtype=np.float64)
+    s = (relu * qs).sum(axis=0) * ks
+    mag = (np.abs(qi).astype(np.float64) @ np.abs(ki).T.astype(np.float64)) * 2.0 ** -18
+    bound = 1e-3 * np.abs(ks) * (np.abs(qs) * mag).sum(axis=0)
+    return s.astype(np.float32), bound
+
+
+def mtp_request_keys(k, k_scale, bt, r, nk):
+    """The first nk keys of request r, gathered through its block table."""
+    nblk = -(-nk // PAGE_TOKENS)
+    blocks = np.asarray(bt[r, :nblk], dtype=np.int64)
+    keys = np.asarray(k)[blocks].reshape(-1, HEAD_DIM)[:nk]
+    ks = np.asarray(k_scale)[blocks].reshape(-1)[:nk]
+    return keys, ks
+
+
+def mtp_scores(q, q_scale, k, k_scale, bt, num_keys, cu_tokens, max_keys, tokens=None):
+    """Scores [T, max_keys] (NaN where not written) and their bounds.
+
+    Token t of request r scores keys [0, min(num_keys[r], max_keys)); there
+    is no causal mask.  ``tokens`` restricts the work to a subset.
+    """
+    T = int(cu_tokens[-1])
+    out = np.full((T, max_keys), np.nan, dtype=np.float32)
+    bound = np.zeros((T, max_keys), dtype=np.float64)
+    want = set(range(T)) if tokens is None else set(int(t) for t in tokens)
+    for r in range(len(num_keys)):
+        toks = [t for t in range(int(cu_tokens[r]), int(cu_tokens[r + 1])) if t in want]
+        if not toks:
+            continue
+        nk = max(0, min(int(num_keys[r]), int(max_keys), bt.shape[1] * PAGE_TOKENS))
+        if nk == 0:
+            continue
+        keys, ks = mtp_request_keys(k, k_scale, bt, r, nk)
+        for t in toks:
+            out[t, :nk], bound[t, :nk] = mtp_token_scores(q[t], q_scale[t], keys, ks)
+    return out, bound
