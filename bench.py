@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse-attention indexer decode path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--quick]
+
+A step is one indexer decode step (score every page below each query's own
+page, then the exact top-16 rows) over the batched-decode workload: 64
+requests, seq_len U[8K, 168K], 8 query slots x 4 index heads x depth 128,
+1,344-column score rows, 1% duplicated pages.  Inputs are synthetic
+(seeded), resident in HBM before the timed region; the 415 MB index-K pool
+is larger than the 129 MB L2, so L2 is not flushed between steps.
+
+The JSON line also carries: the dominant kernel's roofline (decode scorer,
+algorithmic bytes / CUDA-event time, against MEASURED_PEAKS.json), the CPU
+oracle timed on a bounded sample of the same workload, an end-to-end number
+through the C ABI with host buffers (per-step H2D of the queries, scales,
+lengths and block table, D2H of the rows), SM clocks sampled during the
+timed region, and secondary lines for the gather/dequant, long-context and
+multi-token workloads.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica
+of the workload (independent requests, no collective on the data path), the
+reported time is the max over ranks, and value counts all ranks' work.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "indexer decode (query,head,page) scores/s + top-16 rows/s; index-K GB/s vs HBM peak"
+UNIT = "scores/s"
+PAGE_BYTES = 9216
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1946.9)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_nvfp4_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _recorded_traffic(kernel: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/traffic.txt,
+    valid only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = _kernel_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split("#")[0].split()
+            if len(parts) >= 3 and parts[0] == kernel and parts[2] == cur:
+                return float(parts[1])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"idx_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def decode_units(wl) -> dict:
+    """Work of one decode step: (query, head, page) scores, rows, index-K pages."""
+    from sparse_attention_indexer_nvfp4_gb300.workloads import PAGE_TOKENS
+
+    q_len, width, mb = wl["query_len"], wl["width"], wl["max_blocks"]
+    scores = rows = pages = stored = 0
+    for s in wl["seq_lens"]:
+        s = int(s)
+        n = max(0, min((s - 1) // PAGE_TOKENS, mb, width))
+        pages += n
+        for i in range(q_len):
+            own = (s - q_len + i) // PAGE_TOKENS
+            k = max(0, min(own, n))
+            scores += 4 * k
+            stored += 4 * k
+            rows += 4
+    B = len(wl["seq_lens"])
+    # scorer algorithmic bytes: index-K pages + block ids + score stores + queries, scales, lengths
+    score_bytes = pages * (PAGE_BYTES + 4) + stored * 4 + B * (32 * 128 + 32 * 4 + 4)
+    return dict(scores=scores, rows=rows, pages=pages, score_bytes=score_bytes)
+
+
+class Timer:
+    """CUDA-event timing on the launching stream."""
+
+    def __init__(self, torch, stream):
+        self.torch, self.stream = torch, stream
+
+    def run(self, fn, iters: int) -> float:
+        t = self.torch
+        start = t.cuda.Event(enable_timing=True)
+        end = t.cuda.Event(enable_timing=True)
+        t.cuda.synchronize()
+        start.record(self.stream)
+        for _ in range(iters):
+            fn()
+        end.record(self.stream)
+        t.cuda.synchronize()
+        return start.elapsed_time(end) / iters  # ms
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, budget_s: float, seed: int = 0):
+    """Time the oracle on whole pages of the workload until ~budget_s seconds:
+    dequantise the page, score it for all 32 rows, rank a 1,344-column row.
+    Returns (scores per second, pages done, seconds)."""
+    from oracle.indexer import decode_scores, top16
+
+    rng = np.random.default_rng(seed)
+    B = len(wl["seq_lens"])
+    t0 = time.perf_counter()
+    done_scores = pages = 0
+    rows_ranked = 0
+    while time.perf_counter() - t0 < budget_s:
+        b = int(rng.integers(0, B))
+        n = (int(wl["seq_lens"][b]) - 1) // 128
+        js = [int(j) for j in rng.integers(0, n, size=8)]
+        scores, written, _, _ = decode_scores(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"],
+                                              wl["query_len"], wl["width"], wl["max_blocks"],
+                                              pages=[(b, j) for j in js])
+        done_scores += int(written.sum())
+        pages += len(js)
+        row = np.nan_to_num(scores[b, 0], nan=-1.0)
+        top16(row, n)
+        rows_ranked += 1
+    dt = time.perf_counter() - t0
+    return done_scores / dt, pages, dt
+
+
+def run_reference(args, wl, rank: int):
+    if rank != 0:
+        return
+    budget = 4.0 if args.quick else 12.0
+    per_step = []
+    units = 0
+    for s in range(args.warmup + args.steps):
+        rate, pages, dt = oracle_sample(wl, budget / max(1, args.steps + args.warmup), seed=s)
+        if s >= args.warmup:
+            per_step.append((rate, pages, dt))
+    rate = sum(r * d for r, _, d in per_step) / sum(d for _, _, d in per_step)
+    pages = sum(p for _, p, _ in per_step)
+    ms = 1000.0 * sum(d for _, _, d in per_step) / len(per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int64/f64 exact (oracle)", "data": "synthetic",
+        "config": {"workload": "batched decode: 64 requests, seq_len U[8K,168K], 8 slots x 4 heads x 128, "
+                               "1,344-column rows, 1% duplicated pages", "seed": 2},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{pages} random pages (dequant + 32-row scores + one top-16 row each)"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+
+def run_native(args, wl, rank: int, world: int, dist):
+    import torch
+
+    import sparse_attention_indexer_nvfp4_gb300 as idx
+    from sparse_attention_indexer_nvfp4_gb300 import workloads as W
+
+    idx.load_library()
+    dev_idx = torch.cuda.current_device()
+    stream = torch.cuda.current_stream()
+    timer = Timer(torch, stream)
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+
+    def to_dev(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    q, qs, kv, bt, sl = (to_dev(wl[k]) for k in ("q", "q_scale", "kv", "bt", "seq_lens"))
+    B = len(wl["seq_lens"])
+    width, qlen = wl["width"], wl["query_len"]
+    scores = torch.empty((B, 32, width), dtype=torch.float32, device="cuda")
+    out = torch.empty((B, qlen, 4, 16), dtype=torch.int32, device="cuda")
+    ws_bytes = idx.idx_workspace_bytes(B * qlen * 4, width)
+    ws = torch.empty(max(8, ws_bytes) // 8, dtype=torch.int64, device="cuda") if ws_bytes else None
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    units = decode_units(wl)
+    split = ws_bytes > 0
+    launches_per_step = 2 + (1 if split else 0)
+
+    def step():
+        idx.idx_decode_step(q, qs, kv, bt, sl, qlen, scores, out, ws, status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    sampler = ClockSampler(dev_idx)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms = timer.run(step, args.steps)
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    # dominant kernel: the decode scorer, timed alone over the same inputs
+    ms_score = timer.run(lambda: idx.idx_score_pages(q, qs, kv, bt, sl, qlen, scores, status), args.steps)
+    clocks = sampler.stop()
+
+    # end to end through the C ABI with host buffers (pinned), per step
+    h_q = torch.from_numpy(wl["q"]).pin_memory()
+    h_qs = torch.from_numpy(wl["q_scale"]).pin_memory()
+    h_bt = torch.from_numpy(wl["bt"]).pin_memory()
+    h_sl = torch.from_numpy(wl["seq_lens"]).pin_memory()
+    h_out = torch.empty(tuple(out.shape), dtype=torch.int32).pin_memory()
+    d_q, d_qs, d_bt, d_sl = (torch.empty_like(x, device="cuda") for x in (h_q, h_qs, h_bt, h_sl))
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_qs, h_bt, h_sl))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_qs.copy_(h_qs, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        idx.idx_decode_step(d_q, d_qs, kv, d_bt, d_sl, qlen, scores, out, ws, status)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    ms_e2e = timer.run(e2e_step, args.steps)
+    assert torch.equal(h_out, out.cpu())
+
+    extra = {}
+    if not args.quick and rank == 0:
+        extra = secondary(args, torch, idx, W, timer, hbm_peak)
+
+    total_scores = units["scores"] * world
+    value = total_scores / (ms / 1000.0)
+    achieved = units["score_bytes"] / (ms_score / 1000.0) / 1e9
+    traffic = _recorded_traffic("k_score_decode")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32", "data": "synthetic",
+        "config": {
+            "workload": "batched decode: 64 requests, seq_len U[8K,168K], 8 slots x 4 heads x 128, "
+                        "1,344-column rows, 1% duplicated pages (seed 2)",
+            "requests_per_gpu": B, "pages_per_step": units["pages"], "scores_per_step": units["scores"],
+            "index_k_bytes_per_step": units["pages"] * PAGE_BYTES,
+            "l2": "not flushed: the index-K pool (%.0f MB) exceeds the 129 MB L2" % (wl["kv"].nbytes / 1e6),
+            "parallelism": f"replicas x{world}",
+        },
+        "rows_per_s": units["rows"] * world / (ms / 1000.0),
+        "index_k_gbs": units["pages"] * PAGE_BYTES * world / (ms / 1000.0) / 1e9,
+        "index_k_frac_of_hbm": units["pages"] * PAGE_BYTES / (ms / 1000.0) / 1e9 / hbm_peak,
+        "roofline": {
+            "kernel": "k_score_decode", "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": traffic, "peak_kind": peak_kind,
+            "ms_per_launch": ms_score, "algorithmic_bytes_per_launch": units["score_bytes"],
+        },
+        "e2e": {"value": total_scores / (ms_e2e / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "note": "index-K cache resident in HBM (decode state); per-step inputs copied from pinned host"},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "extra": extra,
+    }
+    if rank == 0 and world == 1:
+        budget = 3.0 if args.quick else 12.0
+        rate, pages, dt = oracle_sample(wl, budget)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{pages} random pages of the same workload in {dt:.1f} s "
+                                          "(dequant + 32-row scores each, plus a top-16 row per 8 pages)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def secondary(args, torch, idx, W, timer, hbm_peak) -> dict:
+    """Other workloads of the path, each timed with CUDA events."""
+    res = {}
+    iters = max(3, args.steps // 4)
+
+    def to_dev(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    # gather/dequant: 256 requests, num_pages U[1,1344], 200,000-page pool
+    g = W.gather_workload(seed=1)
+    kv, bt, npg, off = (to_dev(g[k]) for k in ("kv", "bt", "num_pages", "page_offsets"))
+    out = torch.empty((g["out_pages"], 128, 128), dtype=torch.uint8, device="cuda")
+    fn = lambda: idx.idx_dequant_nvfp4_pages(kv, bt, npg, off, g["max_num_pages"], out)
+    fn()
+    ms = timer.run(fn, iters)
+    byts = g["out_pages"] * (PAGE_BYTES + 16384 + 4)
+    res["gather_dequant"] = {"workload": "256 requests, num_pages U[1,1344], 200,000-page pool, 2% special scales",
+                             "ms": ms, "pages_per_s": g["out_pages"] / (ms / 1e3), "gbs": byts / (ms / 1e3) / 1e9,
+                             "frac_of_hbm": byts / (ms / 1e3) / 1e9 / hbm_peak, "launches": 1}
+    del kv, bt, npg, off, out, g
+    torch.cuda.empty_cache()
+
+    # long context: 16 x 500,000 tokens
+    wl = W.long_context()
+    q, qs, kv, bt, sl = (to_dev(wl[k]) for k in ("q", "q_scale", "kv", "bt", "seq_lens"))
+    scores = torch.empty((16, 32, wl["width"]), dtype=torch.float32, device="cuda")
+    out = torch.empty((16, 8, 4, 16), dtype=torch.int32, device="cuda")
+    wsb = idx.idx_workspace_bytes(16 * 32, wl["width"])
+    ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
+    fn = lambda: idx.idx_decode_step(q, qs, kv, bt, sl, 8, scores, out, ws)
+    fn()
+    ms = timer.run(fn, iters)
+    u = decode_units(wl)
+    res["long_context"] = {"workload": "16 requests x 500,000 tokens (3,906 pages), split rows merged",
+                           "ms": ms, "scores_per_s": u["scores"] / (ms / 1e3),
+                           "index_k_gbs": u["pages"] * PAGE_BYTES / (ms / 1e3) / 1e9,
+                           "frac_of_hbm": u["pages"] * PAGE_BYTES / (ms / 1e3) / 1e9 / hbm_peak,
+                           "launches": 2 + (1 if wsb else 0)}
+    del q, qs, kv, bt, sl, scores, out, ws, wl
+    torch.cuda.empty_cache()
+
+    # multi-token scorer + top-16 per token
+    m = W.mtp_workload(seed=3)
+    args_d = [to_dev(m[k]) for k in ("q", "q_scale", "k", "k_scale", "bt", "num_keys", "cu_tokens")]
+    T = int(m["cu_tokens"][-1])
+    o = torch.empty((T, m["max_keys"]), dtype=torch.float32, device="cuda")
+    idx_out = torch.empty((T, 16), dtype=torch.int32, device="cuda")
+    wsb = idx.idx_workspace_bytes(T, m["max_keys"])
+    ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
+
+    def mtp():
+        idx.idx_mtp_score_fp8(*args_d, m["max_keys"], o)
+        idx.idx_topk16_select(o, idx_out, workspace=ws)
+
+    mtp()
+    ms = timer.run(mtp, iters)
+    ms_s = timer.run(lambda: idx.idx_mtp_score_fp8(*args_d, m["max_keys"], o), iters)
+    keys = int(m["num_keys"].sum())
+    flops = 2.0 * T // len(m["num_keys"]) * 64 * 128 * keys
+    kbytes = keys * (128 + 4) + T * (64 * 128 + 64 * 4) + T * m["max_keys"] * 4
+    res["mtp"] = {"workload": "32 requests x 2 tokens x 64 heads, 32,768 keys each; top-16 per token",
+                  "ms": ms, "ms_scorer": ms_s, "token_keys_per_s": T * m["max_keys"] / (ms / 1e3),
+                  "scorer_tflops": flops / (ms_s / 1e3) / 1e12, "scorer_gbs": kbytes / (ms_s / 1e3) / 1e9,
+                  "scorer_frac_of_hbm": kbytes / (ms_s / 1e3) / 1e9 / hbm_peak, "launches": 2 + (1 if wsb else 0)}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip secondary workloads; short CPU baseline")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from sparse_attention_indexer_nvfp4_gb300 import workloads as W
+
+    if args.impl == "reference":
+        if rank == 0:
+            wl = W.batched_decode()
+            run_reference(args, wl, rank)
+        return
+
+    import torch
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        torch.cuda.set_device(local)
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    # each rank runs its own replica (different seed, same shape)
+    wl = W.batched_decode(seed=2 + 1000 * rank)
+    run_native(args, wl, rank, world, dist)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * idx.h - C ABI of the GB300 sparse-attention indexer decode library (libidx.so).
+ *
+ * One hot path: FP8 (E4M3) index queries are scored against a paged NVFP4
+ * index-K cache, and an exact top-16 of pages is selected per (query slot,
+ * index head).  Sources, by page and section:
+ *
+ *   [GATHER]  "vllm.models.minimax_m3.nvidia.ops.gather_nvfp4_index_k",
+ *             module docstring and minimax_m3_gather_nvfp4_index_k_fp8.
+ *   [CP]      "vllm.models.minimax_m3.nvidia.indexer_nvfp4_decode_cp",
+ *             module docstring, _local_topk_push_kernel, _merge_kernel,
+ *             _page_keys, _compact_block_table_kernel.
+ *   [PUBLISH] "wolfcomos/MSA PR #1", sections Summary, Changes, Behaviour
+ *             changes.
+ *   [MTP]     "Mojo module sparse_index_fp8_sm100", module text.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates, frees or synchronises; it only enqueues
+ *     kernels on `stream` (a cudaStream_t; NULL = the legacy default stream),
+ *     so every call can sit inside CUDA-graph capture.
+ *   - Return value: IDX_OK (0) when the work was enqueued (or there was
+ *     nothing to do), else a negative IDX_E_* code; on an error nothing is
+ *     launched.  Argument checks are on the host and never touch the GPU.
+ *   - Empty work (zero requests, rows or pages) returns IDX_OK and launches
+ *     nothing.
+ *   - `status` (may be NULL) is a caller-zeroed int32 in device memory; the
+ *     kernels OR IDX_ST_* bits into it for problems only the device can see
+ *     (for example a block id out of range).  The affected page is skipped;
+ *     no kernel traps.  Read it after the stream completes.
+ *   - Fixed shapes: pages of 128 tokens, index head depth 128, 8 query slots
+ *     and 4 index heads per request for the decode calls.
+ */
+#ifndef IDX_H
+#define IDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---- */
+#define IDX_OK 0
+#define IDX_E_NULL_PTR (-1)        /* a required pointer is NULL */
+#define IDX_E_BAD_SHAPE (-2)       /* a size or stride is negative or inconsistent */
+#define IDX_E_MISALIGNED (-3)      /* a pointer lacks the alignment stated below */
+#define IDX_E_WIDTH_TOO_SMALL (-4) /* score buffer narrower than the call needs */
+#define IDX_E_TOO_LARGE (-5)       /* a size beyond the supported maximum */
+#define IDX_E_CUDA (-6)            /* a CUDA runtime call or launch failed */
+#define IDX_E_WORKSPACE (-7)       /* workspace missing or smaller than idx_workspace_bytes() */
+#define IDX_E_DEVICE (-8)          /* the current device is not an sm_103 GPU */
+
+/* ---- device status bits (OR-ed into *status) ---- */
+#define IDX_ST_BLOCK_OOR 1   /* a block-table entry outside [0, num_blocks): page skipped */
+#define IDX_ST_LEN_CLAMPED 2 /* a request held more pages than the table or buffer: clamped */
+#define IDX_ST_BAD_OUTPUT 4  /* an output page index outside the output buffer: skipped */
+#define IDX_ST_TIMEOUT 8     /* an internal pipeline wait gave up; that CTA's outputs are incomplete */
+
+/* Fixed geometry. */
+#define IDX_PAGE_TOKENS 128
+#define IDX_HEAD_DIM 128
+#define IDX_PAGE_BYTES 9216 /* 128 tokens x (64 code bytes + 8 scale bytes) */
+#define IDX_SLOTS 8
+#define IDX_INDEX_HEADS 4
+#define IDX_TOPK 16
+
+/* Text for a return code. */
+const char* idx_strerror(int code);
+
+/* 1 when the library was built with the QMUL4 dequant instruction
+ * (mul.rn.satfinite.e4m3x4.e2m1x4.e4m3x4), 0 when it uses the exact
+ * fp32-then-round-once path.  Both give identical bytes ([GATHER]). */
+int idx_have_qmul4(void);
+
+/*
+ * Bytes of scratch workspace idx_topk16_select / idx_decode_step need for
+ * `rows` rows of `width` columns (0 when rows fit one CTA each).  Rows longer
+ * than 4,096 columns are split across CTAs whose local top-16s are merged
+ * exactly through this workspace ([CP] module docstring: the global top 16
+ * lies in the union of the partial top 16s).
+ */
+size_t idx_workspace_bytes(int32_t rows, int32_t width);
+
+/*
+ * Gather + dequantise NVFP4 index-K pages into contiguous E4M3 pages [GATHER].
+ *
+ *   kv            [num_blocks, 128, 72] uint8, contiguous, 16-byte aligned.
+ *                 Per page: 8,192 code bytes (token t's 64 bytes at t*64,
+ *                 element d in byte t*64 + d/2, low nibble for even d), then
+ *                 1,024 E4M3 scale bytes, scale (t, g) at 8192 + t*8 + g,
+ *                 g = d/16.  No global scale.
+ *   block_table   [num_reqs, bt_stride] int32; entries [0, max_blocks) used.
+ *   num_pages     [num_reqs] int32: request r gathers its first
+ *                 min(num_pages[r], max_num_pages, max_blocks) logical pages.
+ *   page_offsets  [num_reqs] int32: first output page of request r.
+ *   out           [out_pages, 128, 128] E4M3 bytes, contiguous, 16-byte aligned.
+ *                 out[page_offsets[r] + p][t][d] =
+ *                   e4m3_rn_satfinite(e2m1(code) * e4m3(scale)),
+ *                 a NaN scale gives 0x7F.  Pages not gathered are untouched.
+ * Device checks: block id out of range -> IDX_ST_BLOCK_OOR, output page out
+ * of [0, out_pages) -> IDX_ST_BAD_OUTPUT; the page is skipped.
+ */
+int idx_dequant_nvfp4_pages(const uint8_t* kv, int64_t num_blocks, const int32_t* block_table,
+                            int64_t bt_stride, int32_t max_blocks, const int32_t* num_pages,
+                            const int32_t* page_offsets, int32_t num_reqs, int32_t max_num_pages,
+                            uint8_t* out, int64_t out_pages, int32_t* status, void* stream);
+
+/*
+ * Decode page scores ([CP] module docstring: the Q8KV4 decode scorer's
+ * contract; the page reduction is the max over the page's keys).
+ *
+ *   q             [num_reqs, 8, 4, 128] E4M3 bytes, contiguous, 16-byte aligned;
+ *                 slot s of request b holds query i = s - (8 - query_len).
+ *   q_scale       [num_reqs, 8, 4] float32.
+ *   kv, num_blocks, block_table, bt_stride, max_blocks: as above.
+ *   seq_lens      [num_reqs] int32 tokens per request (the own page included).
+ *   query_len     1..8: the trailing query_len slots are live.
+ *   width         columns of the score buffer.
+ *   scores        [num_reqs, 32, width] float32, row = slot*4 + head.
+ * For request b, pages j < n_b = clamp((seq_len-1)/128, 0, min(max_blocks,
+ * width)) are scored (IDX_ST_LEN_CLAMPED when the clamp bit).  For slot s
+ * (query i) with own page own = floor((seq_len - query_len + i) / 128),
+ *     scores[b][s*4+h][j] = max_t fp32(q_scale[b][s][h] * (q[b][s][h] . K_j[t]))
+ * is stored for j < own only; every other column is left untouched.  K_j is
+ * page bt[b][j] dequantised exactly as in idx_dequant_nvfp4_pages.  A page
+ * with a block id out of range stores NaN (ranked as -inf) and sets
+ * IDX_ST_BLOCK_OOR.  The dot product is accumulated in fp32 on the tensor
+ * cores; the result is within 1e-3 * max_t sum_d |q_scale q_d k_td| of the
+ * exact value.
+ */
+int idx_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
+                    const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                    const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
+                    float* scores, int32_t* status, void* stream);
+
+/*
+ * Exact top-16 per row ([PUBLISH] Changes; [CP] _page_keys).
+ *
+ *   scores        [rows, row_stride] float32, 4-byte aligned; columns [0, width).
+ *   valid_n       [rows] int32 or NULL: row r ranks columns [0, min(valid_n[r], width));
+ *                 NULL ranks all `width` columns.  Negative counts rank nothing.
+ *   force_begin/end  columns in [force_begin, force_end) rank as +inf (empty if end <= begin).
+ *   out_idx       [rows, 16] int32: columns by key descending, -1 padding.
+ *   out_keys      [rows, 16] uint64 or NULL: the keys, 0 padding.  Key =
+ *                 ordered(score) << 32 | (0xFFFFFFFF - column) with
+ *                 ordered(x) = bits(x) ^ (sign ? 0xFFFFFFFF : 0x80000000),
+ *                 after NaN -> -inf, -0 -> +0, forced -> +inf.  So rows sort by
+ *                 score descending, ties to the lower column.
+ *   workspace     device scratch of workspace_bytes >= idx_workspace_bytes(rows, width)
+ *                 (may be NULL when that is 0).  Its contents need no initialisation.
+ */
+int idx_topk16_select(const float* scores, int64_t row_stride, int32_t rows, int32_t width,
+                      const int32_t* valid_n, int32_t force_begin, int32_t force_end, int32_t* out_idx,
+                      uint64_t* out_keys, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One indexer decode step: idx_score_pages, then per (request, query, head)
+ * the output row ([CP] _merge_kernel):
+ *   own + 1 <= 16 : pages 0..own, then -1;
+ *   otherwise     : the 15 best pages below own among those scored, by
+ *                   (score desc, page asc), then own.
+ *   scores_ws     [num_reqs, 32, width] float32 scratch the step scores into
+ *                 (left holding the scores afterwards).
+ *   out           [num_reqs, query_len, 4, 16] int32.
+ *   workspace     >= idx_workspace_bytes(num_reqs * query_len * 4, width) bytes.
+ * Other arguments as in idx_score_pages.
+ */
+int idx_decode_step(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
+                    const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                    const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
+                    float* scores_ws, int32_t* out, void* workspace, size_t workspace_bytes,
+                    int32_t* status, void* stream);
+
+/*
+ * Multi-token FP8 indexer scores [MTP]:
+ *     out[t][key] = k_scale[key] * sum_h relu(q[t][h] . k[key]) * q_scale[t][h]
+ *
+ *   q             [num_tokens, heads, 128] E4M3 bytes, contiguous, 16-byte aligned;
+ *                 heads = 64.
+ *   q_scale       [num_tokens, heads] float32.
+ *   k             [num_blocks, 128, 128] E4M3 bytes (128 keys per block), 16-byte aligned.
+ *   k_scale       [num_blocks, 128] float32.
+ *   block_table   [num_reqs, bt_stride] int32, entries [0, max_blocks) used.
+ *   num_keys      [num_reqs] int32 keys of request r (clamped to max_keys and
+ *                 max_blocks*128).
+ *   cu_tokens     [num_reqs + 1] int32 token offsets; tokens of request r are
+ *                 [cu_tokens[r], cu_tokens[r+1]).  No causal mask.
+ *   out           [num_tokens, max_keys] float32; keys >= num_keys[r] untouched.
+ * Accumulation in fp32 on the tensor cores; within 1e-3 * k_scale *
+ * sum_h |q_scale_h| sum_d |q_hd k_d| of the exact value.
+ */
+int idx_mtp_score_fp8(const uint8_t* q, const float* q_scale, int32_t num_tokens, int32_t heads,
+                      const uint8_t* k, const float* k_scale, int64_t num_blocks, const int32_t* block_table,
+                      int64_t bt_stride, int32_t max_blocks, const int32_t* num_keys, const int32_t* cu_tokens,
+                      int32_t num_reqs, int32_t max_keys, float* out, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDX_H */

@@ -1,0 +1,136 @@
+// Host entry points of the C ABI that are not tied to one kernel file:
+// error text, device check, the decode scorer dispatch and the decode step.
+#include <cstdio>
+
+#include "idx_common.cuh"
+#include "idx_internal.h"
+
+namespace idx {
+
+int launch_score_fma(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
+                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
+                     int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream);
+int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
+                    int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
+                    int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream);
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_device_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 not sm_103
+}  // namespace
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_E_DEVICE;
+  if (dev < 0 || dev >= kMaxDevices) return IDX_E_DEVICE;
+  if (g_device_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return IDX_E_DEVICE;
+    g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return g_device_ok[dev] == 1 ? IDX_OK : IDX_E_DEVICE;
+}
+
+int launch_result() {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return IDX_OK;
+  fprintf(stderr, "libidx: launch failed: %s\n", cudaGetErrorString(e));
+  return IDX_E_CUDA;
+}
+
+// Dense tiles (every (slot, head) row of a request live, 32 rows) go to the
+// tensor-core scorer; a handful of live rows (query_len 1: 4 rows) to the
+// FMA scorer, where a 128 x 32 MMA tile would be mostly idle.
+int launch_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
+                       const int32_t* bt, int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens,
+                       int32_t num_reqs, int32_t query_len, int32_t width, float* scores, int32_t* status,
+                       cudaStream_t stream) {
+  if (query_len * kHeads <= 4)
+    return launch_score_fma(q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks, seq_lens, num_reqs, query_len,
+                            width, scores, status, stream);
+  return launch_score_tc(q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks, seq_lens, num_reqs, query_len, width,
+                         scores, status, stream);
+}
+
+namespace {
+int check_score_args(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
+                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
+                     int32_t query_len, int32_t width, const float* scores) {
+  if (num_reqs < 0 || width < 0 || max_blocks < 0 || num_blocks < 0 || bt_stride < 0) return IDX_E_BAD_SHAPE;
+  if (query_len < 1 || query_len > kSlots) return IDX_E_BAD_SHAPE;
+  if (num_reqs > 65535) return IDX_E_TOO_LARGE;
+  if (!q || !q_scale || !kv || !bt || !seq_lens || !scores) return IDX_E_NULL_PTR;
+  if (bt_stride < max_blocks) return IDX_E_BAD_SHAPE;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(q_scale, 4) || !aligned(bt, 4) || !aligned(seq_lens, 4) ||
+      !aligned(scores, 4))
+    return IDX_E_MISALIGNED;
+  return IDX_OK;
+}
+}  // namespace
+
+}  // namespace idx
+
+extern "C" const char* idx_strerror(int code) {
+  switch (code) {
+    case IDX_OK: return "ok";
+    case IDX_E_NULL_PTR: return "a required pointer is NULL";
+    case IDX_E_BAD_SHAPE: return "a size or stride is negative or inconsistent";
+    case IDX_E_MISALIGNED: return "a pointer lacks the required alignment";
+    case IDX_E_WIDTH_TOO_SMALL: return "the score buffer is narrower than the call needs";
+    case IDX_E_TOO_LARGE: return "a size is beyond the supported maximum";
+    case IDX_E_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case IDX_E_WORKSPACE: return "workspace missing or smaller than idx_workspace_bytes()";
+    case IDX_E_DEVICE: return "the current device is not an sm_103 GPU";
+    default: return "unknown libidx error";
+  }
+}
+
+extern "C" int idx_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
+                               const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                               const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
+                               float* scores, int32_t* status, void* stream) {
+  using namespace idx;
+  if (num_reqs == 0 || width == 0 || max_blocks == 0) {
+    if (num_reqs < 0 || width < 0 || max_blocks < 0 || query_len < 1 || query_len > kSlots) return IDX_E_BAD_SHAPE;
+    return IDX_OK;
+  }
+  int rc = check_score_args(q, q_scale, kv, num_blocks, block_table, bt_stride, max_blocks, seq_lens, num_reqs,
+                            query_len, width, scores);
+  if (rc != IDX_OK) return rc;
+  if ((rc = check_device()) != IDX_OK) return rc;
+  return launch_score_pages(q, q_scale, kv, num_blocks, block_table, bt_stride, max_blocks, seq_lens, num_reqs,
+                            query_len, width, scores, status, (cudaStream_t)stream);
+}
+
+extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
+                               const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
+                               const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
+                               float* scores_ws, int32_t* out, void* workspace, size_t workspace_bytes,
+                               int32_t* status, void* stream) {
+  using namespace idx;
+  if (num_reqs < 0 || width < 0 || max_blocks < 0 || query_len < 1 || query_len > kSlots) return IDX_E_BAD_SHAPE;
+  if (num_reqs == 0) return IDX_OK;
+  if (!out || !seq_lens) return IDX_E_NULL_PTR;
+  if (!aligned(out, 4) || !aligned(workspace, 8)) return IDX_E_MISALIGNED;
+  int rc;
+  const bool any_pages = width > 0 && max_blocks > 0;
+  if (any_pages) {
+    rc = check_score_args(q, q_scale, kv, num_blocks, block_table, bt_stride, max_blocks, seq_lens, num_reqs,
+                          query_len, width, scores_ws);
+    if (rc != IDX_OK) return rc;
+  }
+  const int32_t rows = num_reqs * query_len * kHeads;
+  const size_t need = topk_workspace_bytes(rows, width);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return IDX_E_WORKSPACE;
+  if ((rc = check_device()) != IDX_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (any_pages) {
+    rc = launch_score_pages(q, q_scale, kv, num_blocks, block_table, bt_stride, max_blocks, seq_lens, num_reqs,
+                            query_len, width, scores_ws, status, s);
+    if (rc != IDX_OK) return rc;
+  }
+  DecodeRows d{scores_ws, seq_lens, num_reqs, query_len, width, any_pages ? max_blocks : 0, out};
+  return launch_topk_decode(d, workspace, s);
+}

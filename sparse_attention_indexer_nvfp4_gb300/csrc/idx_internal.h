@@ -1,0 +1,61 @@
+// Host-side helpers shared by the entry points (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "idx.h"
+
+namespace idx {
+
+// IDX_OK when the current device is an sm_103 GPU (cached per device).
+int check_device();
+
+// Map the launch's cudaGetLastError() to a return code.
+int launch_result();
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Columns one warp ranks per pass, and the split of long rows.
+constexpr int kSegCols = 1024;  // 32 columns per lane
+constexpr int kMaxWarpsPerRow = 4;
+
+struct RowSplit {
+  int warps;   // warps per CTA (1, 2 or 4)
+  int nsplit;  // CTAs per row
+};
+
+inline RowSplit row_split(int32_t width) {
+  const int nseg = width <= 0 ? 1 : (int)((width + kSegCols - 1) / kSegCols);
+  const int warps = nseg <= 1 ? 1 : (nseg <= 2 ? 2 : 4);
+  return RowSplit{warps, (nseg + warps - 1) / warps};
+}
+
+inline size_t topk_workspace_bytes(int32_t rows, int32_t width) {
+  if (rows <= 0) return 0;
+  const RowSplit s = row_split(width);
+  if (s.nsplit <= 1) return 0;
+  return (size_t)rows * (size_t)s.nsplit * 16u * sizeof(uint64_t);
+}
+
+// Per-row parameters of the decode selection.
+struct DecodeRows {
+  const float* scores;  // [B, 32, width]
+  const int32_t* seq_lens;
+  int32_t num_reqs, query_len, width, max_blocks;
+  int32_t* out;  // [B, query_len, 4, 16]
+};
+
+int launch_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
+                       const int32_t* bt, int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens,
+                       int32_t num_reqs, int32_t query_len, int32_t width, float* scores, int32_t* status,
+                       cudaStream_t stream);
+
+int launch_topk_plain(const float* scores, int64_t row_stride, int32_t rows, int32_t width, const int32_t* valid_n,
+                      int32_t force_begin, int32_t force_end, int32_t* out_idx, uint64_t* out_keys, void* ws,
+                      cudaStream_t stream);
+
+int launch_topk_decode(const DecodeRows& d, void* ws, cudaStream_t stream);
+
+}  // namespace idx

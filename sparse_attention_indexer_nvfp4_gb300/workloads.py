@@ -151,7 +151,7 @@ def tiny_decode(seed: int = 0) -> dict:
     """1 request of 4,096 tokens: 32 pages, block table a random permutation."""
     rng = rng_for(seed)
     kv = random_nvfp4_pages(rng, 32)
-    bt = rng.permutation(32).astype(np.int32)[None, :]
+    bt = rng.permutation(32).astype(np.int32).reshape(1, 32)
     q = random_e4m3(rng, (1, SLOTS, INDEX_HEADS, HEAD_DIM))
     q_scale = random_uniform_f32(rng, (1, SLOTS, INDEX_HEADS), 0.5, 2.0)
     return dict(kv=kv, bt=bt, seq_lens=np.array([4096], dtype=np.int32), q=q, q_scale=q_scale,

@@ -1,0 +1,82 @@
+"""The C-ABI library loads and exports every symbol include/idx.h declares;
+host-side argument checks answer without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "idx.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(idx_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    from sparse_attention_indexer_nvfp4_gb300 import build
+
+    build.build()
+    import sparse_attention_indexer_nvfp4_gb300 as idx
+
+    return idx
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for want in ("idx_dequant_nvfp4_pages", "idx_score_pages", "idx_topk16_select", "idx_decode_step",
+                 "idx_mtp_score_fp8", "idx_workspace_bytes", "idx_strerror"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(built):
+    lib = ctypes.CDLL(built.library_path())
+    for name in _declared():
+        assert hasattr(lib, name), name
+    # the binding wraps every declared entry point
+    assert set(_declared()) == set(built.SYMBOLS)
+
+
+def test_error_codes_and_strings(built):
+    lib = built.load_library()
+    assert built.idx_strerror(0) == "ok"
+    for code in range(-1, -9, -1):
+        assert built.idx_strerror(code) != "unknown libidx error"
+    # argument checks answer before any CUDA call
+    E_NULL, E_SHAPE, E_MIS, E_WS = -1, -2, -3, -7
+    assert lib.idx_dequant_nvfp4_pages(None, 10, None, 4, 4, None, None, 2, 4, None, 10, None, None) == E_NULL
+    assert lib.idx_dequant_nvfp4_pages(None, 10, None, 4, 4, None, None, -1, 4, None, 10, None, None) == E_SHAPE
+    assert lib.idx_dequant_nvfp4_pages(None, 10, None, 4, 4, None, None, 0, 4, None, 10, None, None) == 0  # empty
+    assert lib.idx_dequant_nvfp4_pages(16, 10, 16, 4, 4, 16, 16, 2, 4, 8, 10, None, None) == E_MIS  # out 8-aligned
+    assert lib.idx_dequant_nvfp4_pages(16, 10, 16, 2, 4, 16, 16, 2, 4, 16, 10, None, None) == E_SHAPE  # stride < width
+    assert lib.idx_score_pages(16, 16, 16, 10, 16, 4, 4, 16, 2, 9, 4, 16, None, None) == E_SHAPE  # query_len 9
+    assert lib.idx_score_pages(16, 16, 16, 10, 16, 4, 4, 16, 2, 0, 4, 16, None, None) == E_SHAPE
+    assert lib.idx_score_pages(8, 16, 16, 10, 16, 4, 4, 16, 2, 8, 4, 16, None, None) == E_MIS  # q not 16-aligned
+    assert lib.idx_score_pages(16, 16, 16, 10, 16, 4, 4, 16, 0, 8, 4, 16, None, None) == 0  # no requests
+    assert lib.idx_topk16_select(16, 5000, 3, 5000, None, 0, 0, None, None, None, 0, None) == E_NULL
+    assert lib.idx_topk16_select(16, 5000, 3, 5000, None, 0, 0, 16, None, None, 0, None) == E_WS
+    assert lib.idx_topk16_select(16, 5000, 3, 5000, None, 0, 0, 16, None, 16, 8, None) == E_WS  # too small
+    assert lib.idx_topk16_select(16, 100, 3, 100, None, 0, 0, 16, 12, None, 0, None) == E_MIS  # keys 8-aligned
+    assert lib.idx_topk16_select(16, 100, 0, 100, None, 0, 0, None, None, None, 0, None) == 0
+    assert lib.idx_mtp_score_fp8(16, 16, 4, 0, 16, 16, 8, 16, 4, 4, 16, 16, 2, 10, 16, None, None) == E_SHAPE
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 5000, 16, 16, None, 0, None, None) == E_WS
+
+
+def test_workspace_sizing(built):
+    # one CTA covers up to 4,096 columns; wider rows split across CTAs
+    assert built.idx_workspace_bytes(100, 1) == 0
+    assert built.idx_workspace_bytes(100, 4096) == 0
+    assert built.idx_workspace_bytes(100, 4097) == 100 * 2 * 16 * 8
+    assert built.idx_workspace_bytes(64, 32768) == 64 * 8 * 16 * 8
+    assert built.idx_workspace_bytes(0, 32768) == 0
+
+
+def test_qmul4_flag_matches_probe(built):
+    from sparse_attention_indexer_nvfp4_gb300 import build
+
+    assert built.idx_have_qmul4() == build.probe_qmul4()
