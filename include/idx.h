@@ -18,7 +18,8 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
  *     library never allocates, frees or synchronises; it only enqueues
  *     kernels on `stream` (a cudaStream_t; NULL = the legacy default stream),
- *     so every call can sit inside CUDA-graph capture.
+ *     so idx_dequant_nvfp4_pages, idx_score_pages, idx_topk16_select,
+ *     idx_decode_step and idx_mtp_score_fp8 can sit inside CUDA-graph capture.
  *   - Return value: IDX_OK (0) when the work was enqueued (or there was
  *     nothing to do), else a negative IDX_E_* code; on an error nothing is
  *     launched.  Argument checks are on the host and never touch the GPU.
@@ -154,6 +155,29 @@ int idx_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, i
 int idx_topk16_select(const float* scores, int64_t row_stride, int32_t rows, int32_t width,
                       const int32_t* valid_n, int32_t force_begin, int32_t force_end, int32_t* out_idx,
                       uint64_t* out_keys, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * idx_topk16_select without a caller workspace, for callers that cannot
+ * allocate device memory (a plugin inside a framework that owns every
+ * device allocation, a serving loop that allows no allocation after
+ * start-up, a captured graph replayed without a memory pool).  The pages
+ * have no counterpart to this entry point; it is a packaging of the
+ * selector above.
+ *
+ * Same arguments and results as idx_topk16_select.  Rows that need more
+ * split-row scratch than IDX_NOALLOC_SCRATCH_BYTES (4 MiB; see
+ * idx_workspace_bytes) are rejected with IDX_E_TOO_LARGE.  The scratch is
+ * a __device__ array inside the library: every GPU that loads the library
+ * holds it until exit, every call shares it (it keeps the last call's
+ * contents; nothing needs clearing), and calls that overlap on the GPU race
+ * on it, so serialise them.  The first call on each device looks up the
+ * array's address (cudaGetSymbolAddress, with that device current); make it
+ * before any stream capture.  No allocation happens in any call.
+ */
+#define IDX_NOALLOC_SCRATCH_BYTES (4u << 20)
+int idx_topk16_select_noalloc(const float* scores, int64_t row_stride, int32_t rows, int32_t width,
+                              const int32_t* valid_n, int32_t force_begin, int32_t force_end, int32_t* out_idx,
+                              uint64_t* out_keys, void* stream);
 
 /*
  * One indexer decode step: idx_score_pages, then per (request, query, head)

@@ -23,6 +23,8 @@ __all__ = [
     "idx_dequant_nvfp4_pages",
     "idx_score_pages",
     "idx_topk16_select",
+    "idx_topk16_select_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
     "idx_decode_step",
     "idx_mtp_score_fp8",
     "SYMBOLS",
@@ -40,6 +42,7 @@ ST_BLOCK_OOR = 1
 ST_LEN_CLAMPED = 2
 ST_BAD_OUTPUT = 4
 ST_TIMEOUT = 8
+NOALLOC_SCRATCH_BYTES = 4 << 20  # scratch inside the library used by idx_topk16_select_noalloc
 
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -54,6 +57,7 @@ SYMBOLS = {
     "idx_dequant_nvfp4_pages": (ctypes.c_int, [_p, _i64, _p, _i64, _i32, _p, _p, _i32, _i32, _p, _i64, _p, _p]),
     "idx_score_pages": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p]),
     "idx_topk16_select": (ctypes.c_int, [_p, _i64, _i32, _i32, _p, _i32, _i32, _p, _p, _p, _sz, _p]),
+    "idx_topk16_select_noalloc": (ctypes.c_int, [_p, _i64, _i32, _i32, _p, _i32, _i32, _p, _p, _p]),
     "idx_decode_step": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p, _sz, _p, _p]),
     "idx_mtp_score_fp8": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _p, _i64, _i32, _p, _p, _i32, _i32, _p, _p, _p]),
 }
@@ -157,6 +161,18 @@ def idx_topk16_select(scores, out_idx, valid_n=None, force_begin: int = 0, force
     return _check("idx_topk16_select", lib.idx_topk16_select(
         _ptr(scores), _row_stride(scores), rows, width, _ptr(valid_n), int(force_begin), int(force_end), _ptr(out_idx),
         _ptr(out_keys), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def idx_topk16_select_noalloc(scores, out_idx, valid_n=None, force_begin: int = 0, force_end: int = 0,
+                              out_keys=None, width: int | None = None, stream=None) -> int:
+    """idx_topk16_select for callers that cannot allocate: the split-row scratch
+    is the library's own device array (at most NOALLOC_SCRATCH_BYTES)."""
+    lib = load_library()
+    rows = scores.shape[0]
+    width = scores.shape[1] if width is None else int(width)
+    return _check("idx_topk16_select_noalloc", lib.idx_topk16_select_noalloc(
+        _ptr(scores), _row_stride(scores), rows, width, _ptr(valid_n), int(force_begin), int(force_end),
+        _ptr(out_idx), _ptr(out_keys), _stream(stream)))
 
 
 def idx_decode_step(q, q_scale, kv, block_table, seq_lens, query_len: int, scores_ws, out, workspace=None,
