@@ -141,25 +141,52 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// try_wait with a suspend-time hint: the warp is parked until the phase
+// completes or about `hint_ns` pass, instead of spinning on the barrier.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after about kWaitLimit * kWaitHintNs (2 s) and
+// returns false.  A caller that gets false records IDX_ST_TIMEOUT and winds
+// its CTA down.  The abort flag (another role's timeout) is checked between
+// suspended polls.
+constexpr uint32_t kWaitHintNs = 20000;
+constexpr uint32_t kWaitLimit = 100000;
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity, kWaitHintNs)) return true;
+  for (uint32_t i = 1; i < kWaitLimit; ++i) {
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (mbar_try_wait(bar, parity, kWaitHintNs)) return true;
+  }
+  return false;
+}
+
+// Spinning variant for roles on a pipeline's critical loop, where waking a
+// suspended warp costs more than the wait: polls without a suspend hint,
+// checks the abort flag every 256 polls, gives up after about 2^26 polls
+// (a few seconds).
+__device__ __forceinline__ bool mbar_try_wait_nosuspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait: gives up after `limit` polls (each try_wait itself blocks for
-// a bounded, hardware-defined time) and returns false.  A caller that gets
-// false records IDX_ST_TIMEOUT and winds its CTA down.
-constexpr uint32_t kWaitLimit = 1u << 22;
-
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (abort_flag != nullptr && *abort_flag) return false;
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
+    if (mbar_try_wait_nosuspend(bar, parity)) return true;
+    if ((i & 255u) == 255u && abort_flag != nullptr && *abort_flag) return false;
   }
   return false;
 }

@@ -7,65 +7,93 @@
 // fp32(q_scale * (q . k)), K dequantised with e4m3_rn_satfinite(e2m1*scale)
 // ("vllm ... ops.gather_nvfp4_index_k", module docstring).
 //
-// Design (HBM-bound on the 9,216-byte page read):
-//   * persistent CTAs; CTA c takes the contiguous slice [P*c/G, P*(c+1)/G)
-//     of all (request, page) pairs, so requests straddle at most two CTAs
-//     and the work is balanced to one page;
-//   * warp 4 (producer) streams raw NVFP4 pages into a 3-stage shared
-//     memory ring with 1-D bulk copies (the 72-byte row is not a legal TMA
-//     box, the whole page is one contiguous 9,216-byte copy);
-//   * warps 0-3 (workers) dequantise each page into a 128B-swizzled K-major
-//     E4M3 tile: per 16-element scale group one 8-byte row of a per-scale
-//     lookup table (built on the device by the exact fp32 round-once rule,
-//     so it is the same function) and two byte permutes per 4 elements;
-//   * warp 5 issues tcgen05.mma kind::f8f6f4, M=128 keys x N=32 (slot,head)
-//     rows x K=128 depth as 4 K=32 steps, accumulating fp32 in one of two
-//     32-column TMEM buffers, and commits to mbarriers;
-//   * the workers drain the accumulator with tcgen05.ld 32x32b (one key per
-//     thread, 32 rows per thread), reduce over keys with redux.sync.max.f32
-//     and across the four warps with shared-memory atomics; the last warp to
-//     arrive applies q_scale and stores the 32 scores.
+// One persistent CTA per SM takes the contiguous slice [P*c/G, P*(c+1)/G) of
+// all (request, page) pairs.  Pages flow through a pipeline of warp roles:
+//
+//   producer (1 warp)   raw NVFP4 page -> 8-stage shared-memory ring, one
+//                       9,216-byte bulk copy per page (a 72-byte row is not a
+//                       legal TMA box); its lanes fetch block ids 32 pages ahead;
+//   dequant (16 warps)  4 groups of 4 warps, group g takes pages i = g (mod 4)
+//                       and owns K tile g: the page becomes a 128B-swizzled
+//                       K-major E4M3 tile, one thread per 32 elements (two scale
+//                       groups of one key) through a per-scale lookup table
+//                       (built on the device by the exact fp32 round-once rule,
+//                       so it is the same function; 16 copies so a half-warp
+//                       reads without bank conflicts), 9 operations per 8
+//                       elements;
+//   MMA (2 warps)       issuer e takes pages i = e (mod 2): tcgen05.mma
+//                       kind::f8f6f4, M=128 x N=128 (keys) x K=128 (four K=32
+//                       steps) into TMEM accumulator i % 4.  MMA issue holds
+//                       its thread until the tensor core accepts the work, so
+//                       one issuer's barrier waits would idle the tensor core;
+//                       two issuers hide each other's waits;
+//   epilogue (4 warps)  warp e takes pages i = e (mod 4) and accumulator e,
+//                       reduces each (slot, head) row's 128 key scores with
+//                       tcgen05.ld.red (the load takes the max), applies q_scale
+//                       and stores the score.  TMEM lanes 0-31 belong to the
+//                       SM's first sub-partition, so these warps are warps 0, 4,
+//                       8 and 12 and the dequant warps live elsewhere.
+//
+// The A operand is the request's 32 query rows in shared memory (8 buffers of
+// 4 KB, 128B-swizzled).  The MMA runs at M=128, so A rows 32-127 are read
+// from the 12 KB that follow the buffer; they only produce accumulator rows
+// 32-127, which nothing reads, and keep TMEM free for four accumulators.
 // q_scale is applied after the max: RN multiplication is monotone, so
 // qs * max_t x_t == max_t RN(qs * x_t) for qs >= 0 (and with min for qs < 0).
 //
-// Every wait is bounded; on a timeout the CTA records IDX_ST_TIMEOUT, winds
-// down, waits for its own copies and MMAs, and frees its TMEM.
+// Every barrier has one waiting role that consumes its phases in order, so
+// parity waits cannot alias.  Every wait is bounded; on a timeout the CTA
+// records IDX_ST_TIMEOUT, winds down, waits for its own copies and MMAs, and
+// frees its TMEM.
 #include "idx_common.cuh"
 #include "idx_internal.h"
 
 namespace idx {
 namespace {
 
-constexpr int kStages = 3;
-constexpr int kWorkerWarps = 4;
-constexpr int kWorkers = kWorkerWarps * 32;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
-constexpr uint32_t kTmemCols = 64;  // two 32-column fp32 accumulators
+constexpr int kStages = 8;      // raw page ring
+constexpr int kGroups = 4;      // dequant groups; group g takes pages i = g (mod 4) and K tile g
+constexpr int kGroupWarps = 4;  // each warp of a group takes a quarter page (32 keys)
+constexpr int kPipe = 4;        // K tiles, accumulators, epilogue warps, ready barriers
+constexpr int kIssuers = 2;     // MMA issuing warps
+constexpr int kQBufs = 8;       // query tiles in shared memory (request k uses k % 8)
+constexpr int kProducerWarp = 22;
+constexpr int kIssuerWarp0 = 20;
+constexpr int kThreads = 23 * 32;
+__host__ __device__ constexpr bool is_epi_warp(int w) { return w < 16 && (w & 3) == 0; }
+// dequant warp index 0..15 of warp w (w in 1-3, 5-7, 9-11, 13-15, 16-19)
+__device__ __forceinline__ int worker_index(int w) { return w < 16 ? w - (w >> 2) - 1 : w - 4; }
+
+constexpr int kMmaM = 128;          // query rows padded to the full datapath
+constexpr int kMmaN = kPageTokens;  // 128 keys
+constexpr uint32_t kAccCols = kMmaN;  // fp32 columns per accumulator
+constexpr uint32_t kTmemCols = 512;   // four accumulators
 // tcgen05 instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B
 // E4M3 (format 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kRows >> 3) << 17) | ((uint32_t)(kPageTokens >> 4) << 24);
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kMmaM >> 4) << 24);
 
 constexpr int kKTile = kPageTokens * kHeadDim;  // 16384
-constexpr int kQTile = kRows * kHeadDim;        // 4096
-constexpr int kOffK = 0;
-constexpr int kOffQ = kOffK + 2 * kKTile;
-constexpr int kOffRaw = kOffQ + 2 * kQTile;
+constexpr int kQTile = kRows * kHeadDim;        // 4096: 32 rows of the A operand
+constexpr int kLutCopies = 16;
+constexpr int kRing = 32;  // page validity and page-done rings (pages in flight stay < 20 apart)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kQBufs * kQTile;  // A rows 32-127 of the last query buffer read K tile 0
+constexpr int kOffRaw = kOffK + kPipe * kKTile;
 constexpr int kOffLut = kOffRaw + kStages * kPageBytes;
-constexpr int kOffPart = kOffLut + 256 * 8;  // [2 parity][max, min][32] int32 + [2] counters
-constexpr int kOffBar = kOffPart + 2 * 2 * 32 * 4 + 16;
-enum Bars { kRawFull = 0, kRawEmpty = kStages, kKtFull = 2 * kStages, kKtEmpty = kKtFull + 2, kAccFull = kKtEmpty + 2,
-            kAccEmpty = kAccFull + 2, kDrain = kAccEmpty + 2, kNumBars };
+constexpr int kOffValid = kOffLut + 256 * 8 * kLutCopies;
+constexpr int kOffDone = kOffValid + kRing * 4;
+constexpr int kOffBar = kOffDone + kRing * 4;
+enum Bars { kRawFull = 0, kRawEmpty = kStages, kReady = 2 * kStages, kKtEmpty = kReady + kPipe, kAccFull = kKtEmpty + kPipe,
+            kDrain = kAccFull + kPipe, kNumBars = kDrain + kIssuers };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
+static_assert(kOffQ + (kQBufs - 1) * kQTile + kMmaM * kHeadDim <= kOffRaw, "A rows 32-127 stay inside the CTA's tiles");
 
 struct Misc {
   uint32_t tmem_base;
   int abort_flag;
   unsigned long long total;
   int b0, j0;
-  int count;
 };
 
 __device__ __forceinline__ int pages_of(int seq, int cap) { return max(0, min(floor_div_page(seq - 1), cap)); }
@@ -78,22 +106,28 @@ struct Cursor {
     seq_lens = sl, B = nb, cap = c, b = b0, j = j0;
     n = b < B ? pages_of(seq_lens[b], cap) : 0;
   }
-  __device__ void next() {
-    ++j;
+  // Move k pages on; returns how many requests with pages were entered.
+  __device__ int advance(int k) {
+    j += k;
+    int entered = 0;
     while (j >= n && b < B) {
+      j -= n;
       ++b;
-      j = 0;
       n = b < B ? pages_of(seq_lens[b], cap) : 0;
+      entered += n > 0;
     }
+    return entered;
   }
 };
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  // K-major, 128-byte swizzle: rows of 128 bytes, 8-row atoms 1,024 bytes apart.
+  // K-major, 128-byte swizzle: rows of 128 bytes, 8-row atoms 1,024 bytes apart
+  // (stride byte offset 1024; the leading offset is unused for this layout).
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T (both K-major, 128-byte swizzle).
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -109,38 +143,21 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ float redux_max(float x) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ float redux_min(float x) {
-  float r;
-  asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-// fp32 <-> int32 whose signed order is the float order
-__device__ __forceinline__ int f2o(float x) {
-  const int i = __float_as_int(x);
-  return i >= 0 ? i : (i ^ 0x7FFFFFFF);
-}
-__device__ __forceinline__ float o2f(int i) { return __int_as_float(i >= 0 ? i : (i ^ 0x7FFFFFFF)); }
+// 16 consecutive fp32 columns of this thread's TMEM lane, reduced (max or
+// min) by the load itself; the loaded values are not used.
+#define IDX_TMEM_LDRED16(OP, taddr, red)                                                                 \
+  do {                                                                                                  \
+    uint32_t r_[16];                                                                                    \
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x16." OP                                          \
+                 ".f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"           \
+                 : "=r"(r_[0]), "=r"(r_[1]), "=r"(r_[2]), "=r"(r_[3]), "=r"(r_[4]), "=r"(r_[5]),        \
+                   "=r"(r_[6]), "=r"(r_[7]), "=r"(r_[8]), "=r"(r_[9]), "=r"(r_[10]), "=r"(r_[11]),     \
+                   "=r"(r_[12]), "=r"(r_[13]), "=r"(r_[14]), "=r"(r_[15]), "=f"(red)                   \
+                 : "r"(taddr));                                                                         \
+    (void)r_;                                                                                           \
+  } while (0)
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
@@ -148,15 +165,19 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
-// Four E2M1 codes (16 bits, element 0 in the low nibble) -> four E4M3 bytes
-// through the scale's table row (lo: magnitudes 0-3, hi: 4-7).  The code's
-// sign flips the product's sign bit: a permute in sign-replicate mode turns
-// each code's bit 3 into 0x80 (positive) or 0xFF (negative); bit 6 of that
-// byte, moved to bit 7, is the sign to apply.
-__device__ __forceinline__ uint32_t dq4_lut(uint32_t codes16, uint32_t lo, uint32_t hi) {
-  const uint32_t mag = prmt(lo, hi, codes16 & 0x7777u);
-  const uint32_t sgn = prmt(0x80808080u, 0x80808080u, codes16 & 0xFFFFu);
-  return mag ^ ((sgn << 1) & 0x80808080u);
+// Eight E2M1 codes (one word, element 0 in the low nibble) -> eight E4M3
+// bytes through the scale's table row (lo: magnitudes 0-3, hi: 4-7), as two
+// words (elements 0-3, 4-7).  Magnitudes: one byte permute per four codes
+// with the sign bits masked off.  Signs: a byte permute in sign-replicate mode
+// copies bit 7 of a byte of w (the odd code's sign) or of w << 4 (the even
+// code's sign) into a whole byte, and bit 7 of that byte flips the product's
+// sign bit.  9 operations per 8 elements.
+__device__ __forceinline__ uint2 dq8_lut(uint32_t w, uint32_t lo, uint32_t hi) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t w4 = w << 4;
+  const uint32_t mag0 = prmt(lo, hi, m), mag1 = prmt(lo, hi, m >> 16);
+  const uint32_t sg0 = prmt(w4, w, 0xD9C8u), sg1 = prmt(w4, w, 0xFBEAu);
+  return make_uint2(mag0 ^ (sg0 & 0x80808080u), mag1 ^ (sg1 & 0x80808080u));
 }
 
 __device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, Misc* misc, int32_t* status) {
@@ -168,7 +189,16 @@ __device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, Misc*
   return false;
 }
 
-__global__ void __launch_bounds__(kThreads) k_score_decode(
+__device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity, Misc* misc, int32_t* status) {
+  if (mbar_spin(bar, parity, &misc->abort_flag)) return true;
+  if (!misc->abort_flag) {
+    misc->abort_flag = 1;
+    report(status, IDX_ST_TIMEOUT);
+  }
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     const uint8_t* __restrict__ q, const float* __restrict__ q_scale, const uint8_t* __restrict__ kv,
     int64_t num_blocks, const int32_t* __restrict__ bt, int64_t bt_stride, int32_t max_blocks,
     const int32_t* __restrict__ seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
@@ -179,9 +209,9 @@ __global__ void __launch_bounds__(kThreads) k_score_decode(
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
-  int* part = reinterpret_cast<int*>(smem + kOffPart);  // [parity][max|min][32]
-  int* part_cnt = part + 2 * 2 * 32;                     // [parity]
   uint2* lut = reinterpret_cast<uint2*>(smem + kOffLut);
+  volatile int* valid_ring = reinterpret_cast<volatile int*>(smem + kOffValid);
+  volatile int* done_ring = reinterpret_cast<volatile int*>(smem + kOffDone);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cap = min(max_blocks, width);
@@ -208,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) k_score_decode(
   const unsigned long long p0 = P * blockIdx.x / gridDim.x, p1 = P * (blockIdx.x + 1) / gridDim.x;
   const int count = (int)(p1 - p0);
   if (count == 0) return;  // uniform across the CTA
-  if (warp == 0) {
+  if (warp == 1) {
     unsigned long long acc = 0;
     for (int base = 0; base < num_reqs; base += 32) {
       const int b = base + lane;
@@ -232,20 +262,22 @@ __global__ void __launch_bounds__(kThreads) k_score_decode(
       acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
   }
-  // ---- set-up: barriers, TMEM, lookup table, partial maxima ----
+  // ---- set-up: barriers, TMEM, lookup table, rings ----
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[kRawFull + s], 1);
-      mbar_init(&bars[kRawEmpty + s], kWorkerWarps);
+      mbar_init(&bars[kRawEmpty + s], kGroupWarps);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars[kKtFull + s], kWorkerWarps);
+    for (int s = 0; s < kPipe; ++s) {
+      // page i is ready for its MMA when its 4 dequant warps arrived and the
+      // epilogue of page i - 4 freed accumulator i % 4 (pre-arrived for i < 4)
+      mbar_init(&bars[kReady + s], kGroupWarps + 1);
       mbar_init(&bars[kKtEmpty + s], 1);
       mbar_init(&bars[kAccFull + s], 1);
-      mbar_init(&bars[kAccEmpty + s], kWorkerWarps);
     }
-    mbar_init(&bars[kDrain], 1);
+    for (int s = 0; s < kIssuers; ++s) mbar_init(&bars[kDrain + s], 1);
     fence_mbar_init();
+    for (int s = 0; s < kPipe; ++s) mbar_arrive(&bars[kReady + s]);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&misc->tmem_base)),
@@ -253,16 +285,13 @@ __global__ void __launch_bounds__(kThreads) k_score_decode(
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid < kWorkers) {
+  if (tid < 256) {
     // table row of scale byte s: e4m3_rn_satfinite(m * e4m3(s)) for the magnitudes m of codes 0..7
-    for (int s = tid; s < 256; s += kWorkers) lut[s] = dequant8_fp32(0x76543210u, e4m3_to_f32((uint32_t)s));
-    if (tid < 64) {
-      const int par = tid >> 5, l = tid & 31;
-      part[par * 64 + l] = (int)0x80000000;  // max slot
-      part[par * 64 + 32 + l] = 0x7FFFFFFF;  // min slot
-    }
-    if (tid < 2) part_cnt[tid] = 0;
+    const uint2 row = dequant8_fp32(0x76543210u, e4m3_to_f32((uint32_t)tid));
+#pragma unroll
+    for (int c = 0; c < kLutCopies; ++c) lut[tid * kLutCopies + c] = row;
   }
+  if (tid < kRing) done_ring[tid] = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -271,173 +300,206 @@ __global__ void __launch_bounds__(kThreads) k_score_decode(
 
   if (warp == kProducerWarp) {
     // ---------------- producer: raw pages into the ring ----------------
-    if (lane == 0) {
-      Cursor cur;
-      cur.init(seq_lens, num_reqs, cap, b0, j0);
-      int issued = 0;
-      for (int i = 0; i < count; ++i) {
-        const int stage = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!timed_wait(&bars[kRawEmpty + stage], ph ^ 1u, misc, status)) break;
-        const int64_t blk = bt[(int64_t)cur.b * bt_stride + cur.j];
-        if (blk >= 0 && blk < num_blocks) {
-          mbar_arrive_expect_tx(&bars[kRawFull + stage], kPageBytes);
-          bulk_g2s(smem + kOffRaw + stage * kPageBytes, kv + blk * kPageBytes, kPageBytes, &bars[kRawFull + stage]);
-        } else {
-          mbar_arrive(&bars[kRawFull + stage]);
-        }
-        issued = i + 1;
-        cur.next();
+    Cursor lc;  // lane k walks pages k, k + 32, k + 64, ...
+    lc.init(seq_lens, num_reqs, cap, b0, j0);
+    lc.advance(lane);
+    int issued = 0;
+    int64_t ids = lane < count ? (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j] : -1;
+    lc.advance(32);
+    bool ok_all = true;
+    for (int base = 0; base < count && ok_all; base += 32) {
+      int64_t ids_next = -1;
+      if (base + 32 < count) {
+        ids_next = base + 32 + lane < count ? (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j] : -1;
+        lc.advance(32);
       }
-      // never leave with a copy in flight
+      const int n = min(32, count - base);
+      for (int k = 0; k < n; ++k) {
+        const int i = base + k;
+        const int64_t blk = __shfl_sync(0xFFFFFFFFu, ids, k);
+        int ok = 1;
+        if (lane == 0) {
+          const int stage = i % kStages;
+          if (timed_wait(&bars[kRawEmpty + stage], ((uint32_t)(i / kStages) & 1u) ^ 1u, misc, status)) {
+            const bool valid = blk >= 0 && blk < num_blocks;
+            valid_ring[i % kRing] = valid ? 1 : 0;
+            if (valid) {
+              mbar_arrive_expect_tx(&bars[kRawFull + stage], kPageBytes);
+              bulk_g2s(smem + kOffRaw + stage * kPageBytes, kv + blk * kPageBytes, kPageBytes,
+                       &bars[kRawFull + stage]);
+            } else {
+              mbar_arrive(&bars[kRawFull + stage]);
+            }
+            issued = i + 1;
+          } else {
+            ok = 0;
+          }
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+          ok_all = false;
+          break;
+        }
+      }
+      ids = ids_next;
+    }
+    // never leave with a copy in flight
+    if (lane == 0)
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_wait(&bars[kRawFull + i % kStages], (uint32_t)(i / kStages) & 1u, nullptr);
-    }
-  } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kIssuers) {
+    // ---------------- MMA issuers ----------------
+    const int e = warp - kIssuerWarp0;
     if (lane == 0) {
       Cursor cur;
       cur.init(seq_lens, num_reqs, cap, b0, j0);
-      int req_ord = -1, prev_b = -1;
-      const uint32_t k_base = sbase + kOffK, q_base = sbase + kOffQ;
+      int req_ord = cur.advance(e);
       bool issued_any = false;
-      for (int i = 0; i < count; ++i) {
-        if (cur.b != prev_b) {
-          ++req_ord;
-          prev_b = cur.b;
-        }
-        const int kt = i & 1;
-        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-        if (!timed_wait(&bars[kKtFull + kt], ph, misc, status)) break;
-        if (!timed_wait(&bars[kAccEmpty + kt], ph ^ 1u, misc, status)) break;
+      for (int i = e; i < count; i += kIssuers) {
+        const int s = i % kPipe;
+        if (!spin_wait(&bars[kReady + s], (uint32_t)(i / kPipe) & 1u, misc, status)) break;
         tc_fence_after();
-        const uint64_t adesc = sw128_desc(k_base + kt * kKTile);
-        const uint64_t bdesc = sw128_desc(q_base + (req_ord & 1) * kQTile);
-        const uint32_t d = tmem + (uint32_t)(kt * kRows);
+        const uint64_t adesc = sw128_desc(sbase + kOffQ + (uint32_t)(req_ord % kQBufs) * kQTile);
+        const uint64_t bdesc = sw128_desc(sbase + kOffK + (uint32_t)s * kKTile);
+        const uint32_t d = tmem + (uint32_t)s * kAccCols;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 32; ++kk) mma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
-        mma_commit(&bars[kAccFull + kt]);
-        mma_commit(&bars[kKtEmpty + kt]);
+        mma_commit(&bars[kAccFull + s]);
+        mma_commit(&bars[kKtEmpty + s]);
         issued_any = true;
-        cur.next();
+        req_ord += cur.advance(kIssuers);
       }
       if (issued_any) {
         // all MMAs issued by this thread complete before TMEM is freed
-        mma_commit(&bars[kDrain]);
-        mbar_wait(&bars[kDrain], 0, nullptr);
+        mma_commit(&bars[kDrain + e]);
+        mbar_wait(&bars[kDrain + e], 0, nullptr);
       }
     }
-  } else {
-    // ---------------- workers: dequant, then the previous page's epilogue ----------------
-    const int g = tid & 7, t0 = tid >> 3;
-    const uint32_t swz = (uint32_t)((g ^ (t0 & 7)) << 4);
+  } else if (is_epi_warp(warp)) {
+    // ---------------- epilogue: lane = (slot, head) row ----------------
+    const int e = warp >> 2;  // pages i = e (mod 4), accumulator e
     Cursor cur;
     cur.init(seq_lens, num_reqs, cap, b0, j0);
-    int req_ord = -1, prev_b = -1;
-    int eb = -1, ej = 0;  // page awaiting its epilogue
-    bool evalid = false;
-    const uint32_t tmem_lane = tmem + ((uint32_t)(warp * 32) << 16);
-
-    auto epilogue = [&](int i, int b, int j, bool valid) -> bool {
-      const int a = i & 1;
-      if (!timed_wait(&bars[kAccFull + a], (uint32_t)(i >> 1) & 1u, misc, status)) return false;
-      tc_fence_after();
-      float v[32];
-      tmem_ld32(tmem_lane + (uint32_t)(a * kRows), v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kAccEmpty + a]);
-      const float qs = q_scale[(int64_t)b * kRows + lane];
-      const bool neg = __any_sync(0xFFFFFFFFu, !(qs >= 0.f));
-      float mx = 0.f, mn = 0.f;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float r = redux_max(v[c]);
-        mx = lane == c ? r : mx;
+    cur.advance(e);
+    const int slot = lane >> 2, iq = slot - (kSlots - query_len);
+    int prev_b = -1, own = -1;
+    float qs = 0.f;
+    bool neg = false;
+    const uint32_t acc = tmem + (uint32_t)e * kAccCols;
+    for (int i = e; i < count; i += kPipe) {
+      const int b = cur.b, j = cur.j;
+      cur.advance(kPipe);
+      if (b != prev_b) {
+        prev_b = b;
+        qs = q_scale[(int64_t)b * kRows + lane];
+        neg = __any_sync(0xFFFFFFFFu, !(qs >= 0.f));
+        own = iq >= 0 ? floor_div_page(seq_lens[b] - query_len + iq) : -1;
       }
-      int* pm = part + a * 64;
-      atomicMax(&pm[lane], f2o(mx));
+      if (!timed_wait(&bars[kAccFull + e], (uint32_t)(i / kPipe) & 1u, misc, status)) break;
+      tc_fence_after();
+      if (lane == 0) done_ring[i % kRing] = i + 1;  // page i's MMA is complete
+      const bool page_ok = valid_ring[i % kRing] != 0;
+      float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+      for (int c = 0; c < (int)kAccCols; c += 16) {
+        float r0;
+        IDX_TMEM_LDRED16("max", acc + (uint32_t)c, r0);
+        tmem_wait_ld();
+        mx = fmaxf(mx, r0);
+      }
       if (neg) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float r = redux_min(v[c]);
-          mn = lane == c ? r : mn;
+        for (int c = 0; c < (int)kAccCols; c += 16) {
+          float r0;
+          IDX_TMEM_LDRED16("min", acc + (uint32_t)c, r0);
+          tmem_wait_ld();
+          mn = fminf(mn, r0);
         }
-        atomicMin(&pm[32 + lane], f2o(mn));
       }
-      __threadfence_block();
+      tc_fence_before();
       __syncwarp();
-      int old = 0;
-      if (lane == 0) old = atomicAdd(&part_cnt[a], 1);
-      old = __shfl_sync(0xFFFFFFFFu, old, 0);
-      if (old == kWorkerWarps - 1) {  // last warp: finish the page
-        __threadfence_block();
-        const float m = o2f(pm[lane]);
-        const float n = o2f(pm[32 + lane]);
-        pm[lane] = (int)0x80000000;
-        pm[32 + lane] = 0x7FFFFFFF;
-        float val = qs >= 0.f ? qs * m : qs * n;
-        if (!valid) val = __int_as_float(0x7FC00000);
-        const int slot = lane >> 2, iq = slot - (kSlots - query_len);
-        const int seq = seq_lens[b];
-        if (iq >= 0 && j < floor_div_page(seq - query_len + iq)) scores[((int64_t)b * kRows + lane) * width + j] = val;
-        __syncwarp();
-        if (lane == 0) part_cnt[a] = 0;
-      }
-      return true;
-    };
-
+      if (lane == 0) mbar_arrive(&bars[kReady + e]);  // accumulator e is free for page i + 4
+      float val = qs >= 0.f ? qs * mx : qs * mn;
+      if (!page_ok) val = __int_as_float(0x7FC00000);  // NaN: ranked as -inf
+      if (j < own) scores[((int64_t)b * kRows + lane) * width + j] = val;
+    }
+  } else if (warp < kIssuerWarp0) {
+    // ---------------- dequant: 4 groups of 4 warps ----------------
+    // group grp takes pages i = grp (mod 4) into K tile grp; warp wg of the
+    // group takes keys [32 wg, 32 wg + 32); a thread takes group pair c of keys
+    // t0 + 8k, k < 4 (16 code bytes = 32 elements, scales 2c and 2c+1 per key).
+    const int widx = worker_index(warp);
+    const int grp = widx / kGroupWarps, wg = widx % kGroupWarps;
+    const int c = lane & 3, t0 = wg * 32 + (lane >> 2);
+    const uint32_t swz0 = (uint32_t)(((2 * c) ^ (t0 & 7)) << 4), swz1 = (uint32_t)(((2 * c + 1) ^ (t0 & 7)) << 4);
+    const uint2* lut_l = lut + (lane & (kLutCopies - 1));
+    uint8_t* kd = smem + kOffK + grp * kKTile;
+    Cursor cur;
+    cur.init(seq_lens, num_reqs, cap, b0, j0);
+    int req_ord = cur.advance(grp);
     bool ok = true;
-    for (int i = 0; i < count && ok; ++i) {
-      const int b = cur.b, j = cur.j;
-      if (b != prev_b) {
-        // new request: its queries into the Q buffer of this request's parity
-        ++req_ord;
-        prev_b = b;
-        uint8_t* qt = smem + kOffQ + (req_ord & 1) * kQTile;
-        const uint8_t* src = q + (int64_t)b * kQTile;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int u = tid + kWorkers * k, r = u >> 3, c = u & 7;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + r * kHeadDim + c * 16);
-          *reinterpret_cast<uint4*>(qt + r * kHeadDim + ((c ^ (r & 7)) << 4)) = v;
-        }
-      }
+    for (int i = grp; i < count && ok; i += kGroups) {
+      const int b = cur.b;
+      const bool first_of_request = cur.j == 0 || i == 0;
       const int stage = i % kStages;
       if (!timed_wait(&bars[kRawFull + stage], (uint32_t)(i / kStages) & 1u, misc, status)) break;
-      const int kt = i & 1;
-      if (!timed_wait(&bars[kKtEmpty + kt], ((uint32_t)(i >> 1) & 1u) ^ 1u, misc, status)) break;
-      const int64_t blk = bt[(int64_t)b * bt_stride + j];
-      const bool valid = blk >= 0 && blk < num_blocks;
-      if (valid) {
-        const uint8_t* rs = smem + kOffRaw + stage * kPageBytes;
-        uint8_t* kd = smem + kOffK + kt * kKTile;
+      if (!timed_wait(&bars[kKtEmpty + grp], ((uint32_t)(i / kGroups) & 1u) ^ 1u, misc, status)) break;
+      if (first_of_request && wg == 0) {
+        // The request's 32 query rows into query buffer req_ord % 8.  Request
+        // req_ord - 8 used that buffer; its pages are <= i - 8, and every page
+        // <= i - 16 is complete (the ring bounds the pages in flight), so the
+        // MMAs of pages i - 16 .. i - 8 are checked.
+        if (req_ord >= kQBufs) {
+          for (int p = max(0, i - 16) + lane; p <= i - 8; p += 32) {
+            uint32_t spins = 0;
+            while (done_ring[p % kRing] != p + 1 && ++spins < (1u << 26))
+              if ((spins & 255u) == 0 && misc->abort_flag) break;
+          }
+          __syncwarp();
+          tc_fence_after();
+        }
+        uint8_t* qt = smem + kOffQ + (req_ord % kQBufs) * kQTile;
+        const uint8_t* src = q + (int64_t)b * kQTile;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const int t = t0 + 16 * k;
-          const uint2 c = *reinterpret_cast<const uint2*>(rs + t * 64 + g * 8);
-          const uint2 L = lut[rs[kCodeBytes + t * 8 + g]];
-          uint4 o;
-          o.x = dq4_lut(c.x, L.x, L.y);
-          o.y = dq4_lut(c.x >> 16, L.x, L.y);
-          o.z = dq4_lut(c.y, L.x, L.y);
-          o.w = dq4_lut(c.y >> 16, L.x, L.y);
-          *reinterpret_cast<uint4*>(kd + t * kHeadDim + swz) = o;
+          const int u = lane + 32 * k, r = u >> 3, cc = u & 7;
+          const uint4 v = *reinterpret_cast<const uint4*>(src + r * kHeadDim + cc * 16);
+          *reinterpret_cast<uint4*>(qt + r * kHeadDim + ((cc ^ (r & 7)) << 4)) = v;
         }
-      } else if (tid == 0) {
+      }
+      if (valid_ring[i % kRing]) {
+        const uint8_t* rs = smem + kOffRaw + stage * kPageBytes;
+#pragma unroll
+        for (int h = 0; h < 4; h += 2) {
+        uint4 cw[4];
+        uint32_t sc[4];
+#pragma unroll
+        for (int k = h; k < h + 2; ++k) {
+          const int t = t0 + 8 * k;
+          cw[k] = *reinterpret_cast<const uint4*>(rs + t * 64 + c * 16);
+          sc[k] = *reinterpret_cast<const uint16_t*>(rs + kCodeBytes + t * 8 + 2 * c);
+        }
+#pragma unroll
+        for (int k = h; k < h + 2; ++k) {
+          const int t = t0 + 8 * k;
+          const uint2 L0 = lut_l[(sc[k] & 0xFFu) * kLutCopies];
+          const uint2 L1 = lut_l[(sc[k] >> 8) * kLutCopies];
+          const uint2 a = dq8_lut(cw[k].x, L0.x, L0.y), bb = dq8_lut(cw[k].y, L0.x, L0.y);
+          const uint2 e2 = dq8_lut(cw[k].z, L1.x, L1.y), f = dq8_lut(cw[k].w, L1.x, L1.y);
+          *reinterpret_cast<uint4*>(kd + t * kHeadDim + swz0) = make_uint4(a.x, a.y, bb.x, bb.y);
+          *reinterpret_cast<uint4*>(kd + t * kHeadDim + swz1) = make_uint4(e2.x, e2.y, f.x, f.y);
+        }
+        }
+      } else if (wg == 0 && lane == 0) {
         report(status, IDX_ST_BLOCK_OOR);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[kRawEmpty + stage]);
-        mbar_arrive(&bars[kKtFull + kt]);
+        mbar_arrive(&bars[kReady + grp]);
       }
-      if (i > 0) ok = epilogue(i - 1, eb, ej, evalid);
-      eb = b, ej = j, evalid = valid;
-      cur.next();
+      req_ord += cur.advance(kGroups);
     }
-    if (ok && !*reinterpret_cast<volatile int*>(&misc->abort_flag)) epilogue(count - 1, eb, ej, evalid);
   }
 
   __syncthreads();
@@ -448,7 +510,6 @@ __global__ void __launch_bounds__(kThreads) k_score_decode(
 }
 
 int g_sms[64];
-int g_occ[64];
 bool g_attr[64];
 
 }  // namespace
@@ -459,18 +520,17 @@ int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, i
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IDX_E_CUDA;
   if (!g_attr[dev]) {
-    if (cudaFuncSetAttribute(k_score_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(k_score_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(k_score_decode, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return IDX_E_CUDA;
     if (cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return IDX_E_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_occ[dev], k_score_decode, kThreads, kSmemBytes) !=
-        cudaSuccess)
-      return IDX_E_CUDA;
-    if (g_occ[dev] < 1) return IDX_E_CUDA;
     g_attr[dev] = true;
   }
   const int64_t upper = (int64_t)num_reqs * (int64_t)min(width, max_blocks);
   if (upper <= 0) return IDX_OK;
-  const int grid = (int)std::min<int64_t>((int64_t)g_sms[dev] * g_occ[dev], upper);
+  // one CTA per SM: each CTA holds all 512 TMEM columns of its SM
+  const int grid = (int)std::min<int64_t>((int64_t)g_sms[dev], upper);
   k_score_decode<<<grid, kThreads, kSmemBytes, stream>>>(q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks,
                                                           seq_lens, num_reqs, query_len, width, scores, status);
   return launch_result();
