@@ -93,13 +93,25 @@ class ClockSampler:
         self.path = os.path.join("/tmp", f"idx_clocks_{os.getpid()}.csv")
 
     def start(self):
+        """Start sampling and return once the first sample is written, so the
+        tool's own start-up does not overlap the timed region."""
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 10.0:
+            self.f.flush()
+            try:
+                if os.path.getsize(self.path) > 0 and open(self.path).read().count("\n") >= 2:
+                    break
+            except OSError:
+                pass
+            time.sleep(0.05)
 
     def stop(self) -> dict | None:
         if self.proc is None:
@@ -275,7 +287,6 @@ def run_native(args, wl, rank: int, world: int, dist):
 
     sampler = ClockSampler(dev_idx)
     sampler.start()
-    time.sleep(0.3)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -426,8 +437,8 @@ def secondary(args, torch, idx, W, timer, hbm_peak) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip secondary workloads; short CPU baseline")
     args = ap.parse_args()

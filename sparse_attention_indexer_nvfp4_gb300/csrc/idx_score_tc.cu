@@ -14,14 +14,17 @@
 //                       9,216-byte bulk copy per page (a 72-byte row is not a
 //                       legal TMA box); its lanes fetch block ids 32 pages ahead;
 //   dequant (16 warps)  4 groups of 4 warps, group g takes pages i = g (mod 4)
-//                       and owns K tile g: the page becomes a 128B-swizzled
+//                       and owns two K tiles (one filled while the MMA reads
+//                       the other): the page becomes a 128B-swizzled
 //                       K-major E4M3 tile, one thread per 32 elements (two scale
 //                       groups of one key) through a per-scale lookup table
 //                       (built on the device by the exact fp32 round-once rule,
-//                       so it is the same function; 16 copies so a half-warp
-//                       reads without bank conflicts), 9 operations per 8
+//                       so it is the same function; 8 copies to spread a
+//                       half-warp's reads over the banks), 9 operations per 8
 //                       elements;
-//   MMA (2 warps)       issuer e takes pages i = e (mod 2): tcgen05.mma
+//   MMA (2 warps)       issuer e takes pages i = e (mod 2); it waits for the
+//                       page's K tile (its 4 dequant warps) and for its
+//                       accumulator (the epilogue of page i - 4), then issues tcgen05.mma
 //                       kind::f8f6f4, M=128 x N=128 (keys) x K=128 (four K=32
 //                       steps) into TMEM accumulator i % 4.  MMA issue holds
 //                       its thread until the tensor core accepts the work, so
@@ -34,7 +37,7 @@
 //                       SM's first sub-partition, so these warps are warps 0, 4,
 //                       8 and 12 and the dequant warps live elsewhere.
 //
-// The A operand is the request's 32 query rows in shared memory (8 buffers of
+// The A operand is the request's 32 query rows in shared memory (2 buffers of
 // 4 KB, 128B-swizzled).  The MMA runs at M=128, so A rows 32-127 are read
 // from the 12 KB that follow the buffer; they only produce accumulator rows
 // 32-127, which nothing reads, and keep TMEM free for four accumulators.
@@ -51,12 +54,14 @@
 namespace idx {
 namespace {
 
-constexpr int kStages = 8;      // raw page ring
-constexpr int kGroups = 4;      // dequant groups; group g takes pages i = g (mod 4) and K tile g
+constexpr int kStages = 8;      // raw page ring; a multiple of kGroups so each stage has one consumer group
+constexpr int kGroups = 4;      // dequant groups; group g takes pages i = g (mod 4)
+constexpr int kGroupTiles = 2;  // K tiles per group: the group fills one while the MMA reads the other
+constexpr int kKTiles = kGroups * kGroupTiles;
 constexpr int kGroupWarps = 4;  // each warp of a group takes a quarter page (32 keys)
-constexpr int kPipe = 4;        // K tiles, accumulators, epilogue warps, ready barriers
+constexpr int kPipe = 4;        // accumulators and epilogue warps
 constexpr int kIssuers = 2;     // MMA issuing warps
-constexpr int kQBufs = 8;       // query tiles in shared memory (request k uses k % 8)
+constexpr int kQBufs = 2;       // query tiles in shared memory (request k uses k % 2)
 constexpr int kProducerWarp = 22;
 constexpr int kIssuerWarp0 = 20;
 constexpr int kThreads = 23 * 32;
@@ -74,20 +79,21 @@ constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kMmaN >> 3) << 17) | ((uint3
 
 constexpr int kKTile = kPageTokens * kHeadDim;  // 16384
 constexpr int kQTile = kRows * kHeadDim;        // 4096: 32 rows of the A operand
-constexpr int kLutCopies = 16;
+constexpr int kLutCopies = 8;  // lane & 7 picks a copy
 constexpr int kRing = 32;  // page validity and page-done rings (pages in flight stay < 20 apart)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBufs * kQTile;  // A rows 32-127 of the last query buffer read K tile 0
-constexpr int kOffRaw = kOffK + kPipe * kKTile;
+constexpr int kOffRaw = kOffK + kKTiles * kKTile;
 constexpr int kOffLut = kOffRaw + kStages * kPageBytes;
 constexpr int kOffValid = kOffLut + 256 * 8 * kLutCopies;
 constexpr int kOffDone = kOffValid + kRing * 4;
 constexpr int kOffBar = kOffDone + kRing * 4;
-enum Bars { kRawFull = 0, kRawEmpty = kStages, kReady = 2 * kStages, kKtEmpty = kReady + kPipe, kAccFull = kKtEmpty + kPipe,
-            kDrain = kAccFull + kPipe, kNumBars = kDrain + kIssuers };
+enum Bars { kRawFull = 0, kRawEmpty = kStages, kKtFull = 2 * kStages, kKtEmpty = kKtFull + kKTiles, kAccFull = kKtEmpty + kKTiles,
+            kAccEmpty = kAccFull + kPipe, kDrain = kAccEmpty + kPipe, kNumBars = kDrain + kIssuers };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
 static_assert(kOffQ + (kQBufs - 1) * kQTile + kMmaM * kHeadDim <= kOffRaw, "A rows 32-127 stay inside the CTA's tiles");
+static_assert(kStages % kGroups == 0, "raw stage s is consumed by group s % kGroups only");
 
 struct Misc {
   uint32_t tmem_base;
@@ -180,6 +186,12 @@ __device__ __forceinline__ uint2 dq8_lut(uint32_t w, uint32_t lo, uint32_t hi) {
   return make_uint2(mag0 ^ (sg0 & 0x80808080u), mag1 ^ (sg1 & 0x80808080u));
 }
 
+// mbarrier arrive issued after `after` is computed (an input of the asm).
+__device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, uint32_t after) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar)), "r"(after)
+               : "memory");
+}
+
 __device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, Misc* misc, int32_t* status) {
   if (mbar_wait(bar, parity, &misc->abort_flag)) return true;
   if (!misc->abort_flag) {
@@ -268,16 +280,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       mbar_init(&bars[kRawFull + s], 1);
       mbar_init(&bars[kRawEmpty + s], kGroupWarps);
     }
+    for (int s = 0; s < kKTiles; ++s) {
+      mbar_init(&bars[kKtFull + s], kGroupWarps);  // the tile's 4 dequant warps
+      mbar_init(&bars[kKtEmpty + s], 1);           // the MMA that read it
+    }
     for (int s = 0; s < kPipe; ++s) {
-      // page i is ready for its MMA when its 4 dequant warps arrived and the
-      // epilogue of page i - 4 freed accumulator i % 4 (pre-arrived for i < 4)
-      mbar_init(&bars[kReady + s], kGroupWarps + 1);
-      mbar_init(&bars[kKtEmpty + s], 1);
-      mbar_init(&bars[kAccFull + s], 1);
+      mbar_init(&bars[kAccFull + s], 1);   // the MMA that wrote it
+      mbar_init(&bars[kAccEmpty + s], 1);  // the epilogue that read it
     }
     for (int s = 0; s < kIssuers; ++s) mbar_init(&bars[kDrain + s], 1);
     fence_mbar_init();
-    for (int s = 0; s < kPipe; ++s) mbar_arrive(&bars[kReady + s]);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&misc->tmem_base)),
@@ -356,15 +368,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       bool issued_any = false;
       for (int i = e; i < count; i += kIssuers) {
         const int s = i % kPipe;
-        if (!spin_wait(&bars[kReady + s], (uint32_t)(i / kPipe) & 1u, misc, status)) break;
+        const int tile = (i % kGroups) * kGroupTiles + (i / kGroups) % kGroupTiles;
+        if (!spin_wait(&bars[kKtFull + tile], (uint32_t)(i / kKTiles) & 1u, misc, status)) break;
+        if (!spin_wait(&bars[kAccEmpty + s], ((uint32_t)(i / kPipe) & 1u) ^ 1u, misc, status)) break;
         tc_fence_after();
         const uint64_t adesc = sw128_desc(sbase + kOffQ + (uint32_t)(req_ord % kQBufs) * kQTile);
-        const uint64_t bdesc = sw128_desc(sbase + kOffK + (uint32_t)s * kKTile);
+        const uint64_t bdesc = sw128_desc(sbase + kOffK + (uint32_t)tile * kKTile);
         const uint32_t d = tmem + (uint32_t)s * kAccCols;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 32; ++kk) mma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kAccFull + s]);
-        mma_commit(&bars[kKtEmpty + s]);
+        mma_commit(&bars[kKtEmpty + tile]);
         issued_any = true;
         req_ord += cur.advance(kIssuers);
       }
@@ -417,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kReady + e]);  // accumulator e is free for page i + 4
+      if (lane == 0) mbar_arrive(&bars[kAccEmpty + e]);  // accumulator e is free for page i + 4
       float val = qs >= 0.f ? qs * mx : qs * mn;
       if (!page_ok) val = __int_as_float(0x7FC00000);  // NaN: ranked as -inf
       if (j < own) scores[((int64_t)b * kRows + lane) * width + j] = val;
@@ -432,24 +446,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     const int c = lane & 3, t0 = wg * 32 + (lane >> 2);
     const uint32_t swz0 = (uint32_t)(((2 * c) ^ (t0 & 7)) << 4), swz1 = (uint32_t)(((2 * c + 1) ^ (t0 & 7)) << 4);
     const uint2* lut_l = lut + (lane & (kLutCopies - 1));
-    uint8_t* kd = smem + kOffK + grp * kKTile;
     Cursor cur;
     cur.init(seq_lens, num_reqs, cap, b0, j0);
     int req_ord = cur.advance(grp);
+    int prev_b = -1;
     bool ok = true;
     for (int i = grp; i < count && ok; i += kGroups) {
       const int b = cur.b;
-      const bool first_of_request = cur.j == 0 || i == 0;
+      // Every group writes the query rows before its own first page of a
+      // request (identical bytes when groups overlap), so the MMA of any page
+      // depends, through that page's K-tile barrier, on a completed write.
+      const bool first_of_request = b != prev_b;
+      prev_b = b;
       const int stage = i % kStages;
       if (!timed_wait(&bars[kRawFull + stage], (uint32_t)(i / kStages) & 1u, misc, status)) break;
-      if (!timed_wait(&bars[kKtEmpty + grp], ((uint32_t)(i / kGroups) & 1u) ^ 1u, misc, status)) break;
+      const int tile = grp * kGroupTiles + (i / kGroups) % kGroupTiles;  // used by pages i, i + 8, ... of this group
+      uint8_t* kd = smem + kOffK + tile * kKTile;
+      if (!timed_wait(&bars[kKtEmpty + tile], ((uint32_t)(i / (kGroups * kGroupTiles)) & 1u) ^ 1u, misc, status)) break;
       if (first_of_request && wg == 0) {
-        // The request's 32 query rows into query buffer req_ord % 8.  Request
-        // req_ord - 8 used that buffer; its pages are <= i - 8, and every page
-        // <= i - 16 is complete (the ring bounds the pages in flight), so the
-        // MMAs of pages i - 16 .. i - 8 are checked.
+        // The request's 32 query rows into query buffer req_ord % 2.  Request
+        // req_ord - 2 used that buffer; its pages are < the first page of
+        // request req_ord - 1 <= i - 1, so they are <= i - 2, and every page
+        // <= i - 20 is complete (the raw ring, K tiles and accumulators bound
+        // the pages in flight), so the MMAs of pages i - 20 .. i - 2 are checked.
         if (req_ord >= kQBufs) {
-          for (int p = max(0, i - 16) + lane; p <= i - 8; p += 32) {
+          for (int p = max(0, i - 20) + lane; p <= i - 2; p += 32) {
             uint32_t spins = 0;
             while (done_ring[p % kRing] != p + 1 && ++spins < (1u << 26))
               if ((spins & 255u) == 0 && misc->abort_flag) break;
@@ -466,20 +487,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
           *reinterpret_cast<uint4*>(qt + r * kHeadDim + ((cc ^ (r & 7)) << 4)) = v;
         }
       }
-      if (valid_ring[i % kRing]) {
+      // codes and scales into registers, then the raw stage goes back to the
+      // producer before the (longer) dequantisation
+      const bool page_valid = valid_ring[i % kRing] != 0;
+      uint4 cw[4];
+      uint32_t sc[4];
+      if (page_valid) {
         const uint8_t* rs = smem + kOffRaw + stage * kPageBytes;
 #pragma unroll
-        for (int h = 0; h < 4; h += 2) {
-        uint4 cw[4];
-        uint32_t sc[4];
-#pragma unroll
-        for (int k = h; k < h + 2; ++k) {
+        for (int k = 0; k < 4; ++k) {
           const int t = t0 + 8 * k;
           cw[k] = *reinterpret_cast<const uint4*>(rs + t * 64 + c * 16);
           sc[k] = *reinterpret_cast<const uint16_t*>(rs + kCodeBytes + t * 8 + 2 * c);
         }
+      }
+      // The stage may be refilled only after the loads have returned: the ballot
+      // reads a value computed from every load's result in every lane, and the
+      // warp issues in order, so lane 0's arrive comes after all of them.
+      uint32_t dep = 0;
+      if (page_valid) dep = cw[0].x ^ cw[1].x ^ cw[2].x ^ cw[3].x ^ sc[0] ^ sc[1] ^ sc[2] ^ sc[3];
+      const uint32_t loaded = __ballot_sync(0xFFFFFFFFu, dep == 0u);
+      if (lane == 0) mbar_arrive_after(&bars[kRawEmpty + stage], loaded);
+      if (page_valid) {
 #pragma unroll
-        for (int k = h; k < h + 2; ++k) {
+        for (int k = 0; k < 4; ++k) {
           const int t = t0 + 8 * k;
           const uint2 L0 = lut_l[(sc[k] & 0xFFu) * kLutCopies];
           const uint2 L1 = lut_l[(sc[k] >> 8) * kLutCopies];
@@ -488,16 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
           *reinterpret_cast<uint4*>(kd + t * kHeadDim + swz0) = make_uint4(a.x, a.y, bb.x, bb.y);
           *reinterpret_cast<uint4*>(kd + t * kHeadDim + swz1) = make_uint4(e2.x, e2.y, f.x, f.y);
         }
-        }
       } else if (wg == 0 && lane == 0) {
         report(status, IDX_ST_BLOCK_OOR);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[kRawEmpty + stage]);
-        mbar_arrive(&bars[kReady + grp]);
-      }
+      if (lane == 0) mbar_arrive(&bars[kKtFull + tile]);
       req_ord += cur.advance(kGroups);
     }
   }

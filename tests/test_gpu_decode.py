@@ -184,3 +184,42 @@ def test_long_context_decode(lib):
                                            wl["width"], wl["max_blocks"], pages=pairs)
     err = np.abs(s[written].astype(np.float64) - ref[written].astype(np.float64))
     assert (err <= bound[written]).all()
+
+
+def test_many_short_requests_and_repeatability(lib):
+    """300 requests of 1-30 pages: every CTA crosses request boundaries and
+    reuses its query buffers.  Scores match the oracle once and then stay
+    bit-identical over 30 repeated launches (a pipeline race would show as a
+    run-to-run difference)."""
+    rng = np.random.default_rng(44)
+    seq = rng.integers(129, 3900, size=300).astype(np.int32)
+    wl = W.decode_workload(44, 300, 0, 0, width=32, max_blocks=32, seq_lens=seq, dup_frac=0.05)
+    s, out, st = _step(lib, wl)
+    assert st == 0
+    _check_step(wl, s, out)
+    a = decode_args(wl)
+    first = None
+    for _ in range(30):
+        scores = sentinel_f32((300, 32, 32))
+        lib.idx_score_pages(a["q"], a["q_scale"], a["kv"], a["block_table"], a["seq_lens"], 8, scores)
+        torch.cuda.synchronize()
+        cur = host(scores).view(np.int32)
+        if first is None:
+            first = cur
+            assert np.array_equal(first, s.view(np.int32))
+        assert np.array_equal(cur, first)
+
+
+@pytest.mark.slow
+def test_full_batched_decode_repeatability(lib):
+    """The benchmark workload's scores are bit-identical over 20 launches."""
+    wl = W.batched_decode()
+    a = decode_args(wl)
+    first = None
+    for _ in range(20):
+        scores = sentinel_f32((64, 32, wl["width"]))
+        lib.idx_score_pages(a["q"], a["q_scale"], a["kv"], a["block_table"], a["seq_lens"], 8, scores)
+        cur = scores.view(torch.int32).clone()
+        if first is None:
+            first = cur
+        assert torch.equal(cur, first)
