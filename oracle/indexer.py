@@ -321,12 +321,19 @@ def mtp_token_scores(q_tok, q_scale_tok, k_keys, k_scale_keys):
 
 
 def mtp_request_keys(k, k_scale, bt, r, nk):
-    """The first nk keys of request r, gathered through its block table."""
+    """The first nk keys of request r, gathered through its block table.
+
+    Returns (keys, k_scale, valid): a block id outside [0, num_blocks) gives
+    keys that are not scored (valid False), as in the page-gather step.
+    """
     nblk = -(-nk // PAGE_TOKENS)
     blocks = np.asarray(bt[r, :nblk], dtype=np.int64)
-    keys = np.asarray(k)[blocks].reshape(-1, HEAD_DIM)[:nk]
-    ks = np.asarray(k_scale)[blocks].reshape(-1)[:nk]
-    return keys, ks
+    ok = (blocks >= 0) & (blocks < np.asarray(k).shape[0])
+    safe = np.where(ok, blocks, 0)
+    keys = np.asarray(k)[safe].reshape(-1, HEAD_DIM)[:nk]
+    ks = np.asarray(k_scale)[safe].reshape(-1)[:nk]
+    valid = np.repeat(ok, PAGE_TOKENS)[:nk]
+    return keys, ks, valid
 
 
 def mtp_scores(q, q_scale, k, k_scale, bt, num_keys, cu_tokens, max_keys, tokens=None):
@@ -346,7 +353,9 @@ def mtp_scores(q, q_scale, k, k_scale, bt, num_keys, cu_tokens, max_keys, tokens
         nk = max(0, min(int(num_keys[r]), int(max_keys), bt.shape[1] * PAGE_TOKENS))
         if nk == 0:
             continue
-        keys, ks = mtp_request_keys(k, k_scale, bt, r, nk)
+        keys, ks, valid = mtp_request_keys(k, k_scale, bt, r, nk)
         for t in toks:
-            out[t, :nk], bound[t, :nk] = mtp_token_scores(q[t], q_scale[t], keys, ks)
+            s, b = mtp_token_scores(q[t], q_scale[t], keys, ks)
+            out[t, :nk] = np.where(valid, s, np.float32(np.nan))
+            bound[t, :nk] = np.where(valid, b, 0.0)
     return out, bound

@@ -58,4 +58,12 @@ int launch_topk_plain(const float* scores, int64_t row_stride, int32_t rows, int
 
 int launch_topk_decode(const DecodeRows& d, void* ws, cudaStream_t stream);
 
+// Multi-token scorer on the tensor cores (64 heads); see mtp_tc_supported for the shapes it takes.
+bool mtp_tc_supported(const uint8_t* q, const float* q_scale, const uint8_t* k, const float* k_scale, int32_t heads,
+                      int32_t num_tokens, int64_t num_blocks);
+int launch_mtp_tc(const uint8_t* q, const float* q_scale, int32_t num_tokens, const uint8_t* k, const float* k_scale,
+                  int64_t num_blocks, const int32_t* bt, int64_t bt_stride, int32_t max_blocks, const int32_t* num_keys,
+                  const int32_t* cu_tokens, int32_t num_reqs, int32_t max_keys, float* out, int32_t* status,
+                  cudaStream_t stream);
+
 }  // namespace idx

@@ -97,6 +97,9 @@ extern "C" int idx_mtp_score_fp8(const uint8_t* q, const float* q_scale, int32_t
     return IDX_E_MISALIGNED;
   int rc = check_device();
   if (rc != IDX_OK) return rc;
+  if (mtp_tc_supported(q, q_scale, k, k_scale, heads, num_tokens, num_blocks))
+    return launch_mtp_tc(q, q_scale, num_tokens, k, k_scale, num_blocks, block_table, bt_stride, max_blocks, num_keys,
+                         cu_tokens, num_reqs, max_keys, out, status, (cudaStream_t)stream);
   return launch_mtp_fma(q, q_scale, num_tokens, heads, k, k_scale, num_blocks, block_table, bt_stride, max_blocks, num_keys,
                         cu_tokens, num_reqs, max_keys, out, status, (cudaStream_t)stream);
 }

@@ -1,0 +1,391 @@
+// Multi-token FP8 indexer scores on the tensor cores (tcgen05 + TMA, sm_103a).
+//
+// "Mojo module sparse_index_fp8_sm100", module text:
+//     score[t][key] = k_scale[key] * sum_h relu(q[t][h] . k[key]) * q_scale[t][h]
+// with the depth-128 dot products on the tensor cores: MMA_M = 128 keys (A =
+// the key tile), MMA_N = 128 = 2 tokens x 64 heads (B = the query rows,
+// S^T = K Q^T), MMA_K = 128 depth, fp32 accumulation in TMEM; the epilogue
+// drains one key row per thread, applies relu and q_scale per column, sums
+// each token's 64 head columns in registers, multiplies by k_scale and
+// stores 32 consecutive keys per warp (128-byte stores).
+//
+// Work items are (request, token pair, 128-key block) in that order; one
+// persistent CTA (two per SM) takes a contiguous slice.  Roles:
+//   producer (warp 4)  TMA: the key block [128 keys, 128 B] and the token
+//                      pair's query rows [128, 128 B] with 128-byte swizzle
+//                      straight into the layout the tensor core reads, plus
+//                      k_scale and q_scale by 1-D bulk copies;
+//   MMA (warp 5)       one tcgen05.mma group (4 x K=32) per item into one of
+//                      two 128-column accumulators;
+//   epilogue (warps 0-3) warp w owns keys 32w..32w+31 (TMEM lane quarter w).
+// Every barrier's phases are consumed in order by each role that waits on it;
+// the epilogue also waits on the (already complete) copy barriers of the
+// tiles it reads scales from, which cannot run two phases ahead of it
+// because it releases those buffers itself.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "idx_common.cuh"
+#include "idx_internal.h"
+#include "idx_tc.cuh"
+
+namespace idx {
+namespace {
+
+constexpr int kHeadsTc = 64;
+constexpr int kTokTile = 2;                  // tokens per MMA (N = 2 x 64 = 128)
+constexpr int kStages = 4;                   // key-block ring
+constexpr int kQBufsM = 2;                   // query tiles (one per token pair in flight)
+constexpr int kKTileBytes = kPageTokens * kHeadDim;   // 16384
+constexpr int kQTileBytes = kTokTile * kHeadsTc * kHeadDim;  // 16384
+constexpr int kKsBytes = kPageTokens * 4;    // 512
+constexpr int kQsBytes = kTokTile * kHeadsTc * 4;  // 512
+constexpr int kRingM = 32;
+constexpr int kThreadsM = 6 * 32;
+constexpr int kProdWarp = 4, kMmaWarpM = 5;
+constexpr uint32_t kAccColsM = 128, kTmemColsM = 256;
+constexpr uint32_t kIdescM = idesc_f8(128, kTokTile * kHeadsTc);
+
+constexpr int kOffKm = 0;
+constexpr int kOffQm = kOffKm + kStages * kKTileBytes;
+constexpr int kOffKs = kOffQm + kQBufsM * kQTileBytes;
+constexpr int kOffQs = kOffKs + kStages * kKsBytes;
+constexpr int kOffValidM = kOffQs + kQBufsM * kQsBytes;
+constexpr int kOffBarM = kOffValidM + kRingM * 4;
+enum BarsM { kKFull = 0, kKEmpty = kStages, kQFull = 2 * kStages, kQEmpty = kQFull + kQBufsM,
+             kAFull = kQEmpty + kQBufsM, kAEmpty = kAFull + 2, kDrainM = kAEmpty + 2, kNumBarsM };
+constexpr int kOffMiscM = kOffBarM + kNumBarsM * 8;
+constexpr int kSmemM = kOffMiscM + 64 + 1024;
+
+struct MiscM {
+  uint32_t tmem_base;
+  int abort_flag;
+  unsigned long long total;
+  int r0, rem0;
+};
+
+struct ReqShape {
+  const int32_t* num_keys;
+  const int32_t* cu_tokens;
+  int R, num_tokens, key_cap;
+  __device__ int nk(int r) const { return max(0, min(num_keys[r], key_cap)); }
+  __device__ int tok0(int r) const { return max(0, min(cu_tokens[r], num_tokens)); }
+  __device__ int ntok(int r) const { return max(0, min(cu_tokens[r + 1], num_tokens) - tok0(r)); }
+  __device__ int nkb(int r) const { return (nk(r) + kPageTokens - 1) / kPageTokens; }
+  __device__ int ntt(int r) const { return (ntok(r) + kTokTile - 1) / kTokTile; }
+  __device__ int items(int r) const { return nkb(r) * ntt(r); }
+};
+
+// Cursor over (request, token pair, key block), key block fastest.
+struct ItemCursor {
+  ReqShape sh;
+  int r, tt, kb, n_kb, n_tt;
+  __device__ void load() {
+    n_kb = r < sh.R ? sh.nkb(r) : 0;
+    n_tt = r < sh.R ? sh.ntt(r) : 0;
+  }
+  __device__ void init(const ReqShape& s, int r0, int rem) {
+    sh = s;
+    r = r0;
+    load();
+    tt = n_kb ? rem / n_kb : 0;
+    kb = n_kb ? rem % n_kb : 0;
+  }
+  __device__ void next() {
+    if (++kb < n_kb) return;
+    kb = 0;
+    if (++tt < n_tt) return;
+    tt = 0;
+    do {
+      ++r;
+      load();
+    } while (r < sh.R && n_kb * n_tt == 0);
+  }
+};
+
+__global__ void __launch_bounds__(kThreadsM) k_mtp_tc(const __grid_constant__ CUtensorMap kmap,
+                                                      const __grid_constant__ CUtensorMap qmap,
+                                                      const float* __restrict__ q_scale,
+                                                      const float* __restrict__ k_scale, int64_t num_blocks,
+                                                      const int32_t* __restrict__ bt, int64_t bt_stride,
+                                                      ReqShape shape, int32_t max_keys, float* __restrict__ out,
+                                                      int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBarM);
+  MiscM* misc = reinterpret_cast<MiscM*>(smem + kOffMiscM);
+  volatile int* valid_ring = reinterpret_cast<volatile int*>(smem + kOffValidM);
+  volatile int* abort_flag = &misc->abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    misc->total = 0;
+    misc->abort_flag = 0;
+  }
+  __syncthreads();
+  {
+    unsigned long long local = 0;
+    for (int r = tid; r < shape.R; r += kThreadsM) local += (unsigned long long)shape.items(r);
+    if (local) atomicAdd(&misc->total, local);
+  }
+  __syncthreads();
+  const unsigned long long W = misc->total;
+  const unsigned long long w0 = W * blockIdx.x / gridDim.x, w1 = W * (blockIdx.x + 1) / gridDim.x;
+  const int count = (int)(w1 - w0);
+  if (count == 0) return;
+  if (warp == 1) {
+    unsigned long long acc = 0;
+    for (int base = 0; base < shape.R; base += 32) {
+      const int r = base + lane;
+      const unsigned long long n = r < shape.R ? (unsigned long long)shape.items(r) : 0ull;
+      unsigned long long incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned long long excl = incl - n;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, n > 0 && acc + excl <= w0 && w0 < acc + incl);
+      if (m) {
+        if (lane == __ffs(m) - 1) {
+          misc->r0 = r;
+          misc->rem0 = (int)(w0 - (acc + excl));
+        }
+        break;
+      }
+      acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[kKFull + s], 1);
+      mbar_init(&bars[kKEmpty + s], 1 + 4);  // the MMA (commit) and the 4 epilogue warps (k_scale read)
+    }
+    for (int s = 0; s < kQBufsM; ++s) {
+      mbar_init(&bars[kQFull + s], 1);
+      mbar_init(&bars[kQEmpty + s], 1 + 4);  // the MMA leaving the tile and the 4 epilogue warps
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kAFull + s], 1);
+      mbar_init(&bars[kAEmpty + s], 4);
+    }
+    mbar_init(&bars[kDrainM], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&misc->tmem_base, kTmemColsM);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+  const int r0 = misc->r0, rem0 = misc->rem0;
+
+  if (warp == kProdWarp) {
+    if (lane == 0) {
+      ItemCursor cur;
+      cur.init(shape, r0, rem0);
+      int qord = -1, pr = -1, ptt = -1, issued = 0;  // qord: query tiles issued - 1
+      for (int i = 0; i < count; ++i) {
+        if (cur.r != pr || cur.tt != ptt) {
+          const int qb = (qord + 1) % kQBufsM;
+          if (!timed_wait_flag(&bars[kQEmpty + qb], ((uint32_t)((qord + 1) / kQBufsM) & 1u) ^ 1u, abort_flag, status))
+            break;
+          pr = cur.r, ptt = cur.tt;
+          ++qord;
+          const int t0 = shape.tok0(cur.r) + kTokTile * cur.tt;
+          const int nt = min(kTokTile, shape.ntok(cur.r) - kTokTile * cur.tt);
+          mbar_arrive_expect_tx(&bars[kQFull + qb], kQTileBytes + nt * kHeadsTc * 4);
+          tma_load_2d(smem + kOffQm + qb * kQTileBytes, &qmap, 0, t0 * kHeadsTc, &bars[kQFull + qb]);
+          bulk_g2s(smem + kOffQs + qb * kQsBytes, q_scale + (int64_t)t0 * kHeadsTc, nt * kHeadsTc * 4,
+                   &bars[kQFull + qb]);
+        }
+        const int stage = i % kStages;
+        if (!timed_wait_flag(&bars[kKEmpty + stage], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort_flag, status)) break;
+        const int64_t blk = bt[(int64_t)cur.r * bt_stride + cur.kb];
+        const bool valid = blk >= 0 && blk < num_blocks;
+        valid_ring[i % kRingM] = valid ? 1 : 0;
+        if (valid) {
+          mbar_arrive_expect_tx(&bars[kKFull + stage], kKTileBytes + kKsBytes);
+          tma_load_2d(smem + kOffKm + stage * kKTileBytes, &kmap, 0, (int)(blk * kPageTokens), &bars[kKFull + stage]);
+          bulk_g2s(smem + kOffKs + stage * kKsBytes, k_scale + blk * kPageTokens, kKsBytes, &bars[kKFull + stage]);
+        } else {
+          report(status, IDX_ST_BLOCK_OOR);
+          mbar_arrive(&bars[kKFull + stage]);
+        }
+        issued = i + 1;
+        cur.next();
+      }
+      // never leave with a copy in flight: the last uses of every stage and query buffer
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_wait(&bars[kKFull + i % kStages], (uint32_t)(i / kStages) & 1u, nullptr);
+      for (int qo = max(0, qord - kQBufsM + 1); qo <= qord; ++qo)
+        mbar_wait(&bars[kQFull + qo % kQBufsM], (uint32_t)(qo / kQBufsM) & 1u, nullptr);
+    }
+  } else if (warp == kMmaWarpM) {
+    if (lane == 0) {
+      ItemCursor cur;
+      cur.init(shape, r0, rem0);
+      int qord = -1, pr = -1, ptt = -1;
+      bool issued_any = false;
+      for (int i = 0; i < count; ++i) {
+        if (cur.r != pr || cur.tt != ptt) {
+          pr = cur.r, ptt = cur.tt;
+          if (qord >= 0) mma_commit(&bars[kQEmpty + qord % kQBufsM]);  // the previous query tile is done
+          ++qord;
+          if (!spin_wait_flag(&bars[kQFull + qord % kQBufsM], (uint32_t)(qord / kQBufsM) & 1u, abort_flag, status)) break;
+        }
+        const int stage = i % kStages, a = i & 1;
+        if (!spin_wait_flag(&bars[kKFull + stage], (uint32_t)(i / kStages) & 1u, abort_flag, status)) break;
+        if (!spin_wait_flag(&bars[kAEmpty + a], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, status)) break;
+        tc_fence_after();
+        const uint64_t adesc = sw128_desc(sbase + kOffKm + stage * kKTileBytes);
+        const uint64_t bdesc = sw128_desc(sbase + kOffQm + (qord % kQBufsM) * kQTileBytes);
+        const uint32_t d = tmem + (uint32_t)a * kAccColsM;
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 32; ++kk) mma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, kIdescM, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kAFull + a]);
+        mma_commit(&bars[kKEmpty + stage]);
+        issued_any = true;
+        cur.next();
+      }
+      if (issued_any) {
+        mma_commit(&bars[kDrainM]);
+        mbar_wait(&bars[kDrainM], 0, nullptr);
+      }
+    }
+  } else if (warp < 4) {
+    // epilogue: warp w owns keys 32w + lane of each block (TMEM lane quarter w)
+    ItemCursor cur;
+    cur.init(shape, r0, rem0);
+    int qord = -1, pr = -1, ptt = -1;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    for (int i = 0; i < count; ++i) {
+      const int r = cur.r, tt = cur.tt, kb = cur.kb;
+      cur.next();
+      if (r != pr || tt != ptt) {
+        pr = r, ptt = tt;
+        __syncwarp();
+        if (qord >= 0 && lane == 0) mbar_arrive(&bars[kQEmpty + qord % kQBufsM]);  // done with its q_scale
+        ++qord;
+        // acquire the query tile's q_scale copy (already complete: the MMA waited for it first)
+        const bool ok = timed_wait_flag(&bars[kQFull + qord % kQBufsM], (uint32_t)(qord / kQBufsM) & 1u, abort_flag, status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      }
+      const int stage = i % kStages, a = i & 1;
+      {
+        // the accumulator, then the stage's k_scale copy and validity flag
+        bool ok = timed_wait_flag(&bars[kAFull + a], (uint32_t)(i >> 1) & 1u, abort_flag, status);
+        ok = ok && timed_wait_flag(&bars[kKFull + stage], (uint32_t)(i / kStages) & 1u, abort_flag, status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      }
+      tc_fence_after();
+      const float ks = reinterpret_cast<const float*>(smem + kOffKs + stage * kKsBytes)[warp * 32 + lane];
+      const bool valid = valid_ring[i % kRingM] != 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kKEmpty + stage]);  // k_scale read (the MMA commit is the other arrival)
+      const float4* qs4 = reinterpret_cast<const float4*>(smem + kOffQs + (qord % kQBufsM) * kQsBytes);
+      float acc[kTokTile] = {0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + (uint32_t)a * kAccColsM + (uint32_t)(c * 32), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 s = qs4[(c * 32 + e) / 4];
+          float t = acc[c >> 1];
+          t = fmaf(fmaxf(__uint_as_float(v[e]), 0.f), s.x, t);
+          t = fmaf(fmaxf(__uint_as_float(v[e + 1]), 0.f), s.y, t);
+          t = fmaf(fmaxf(__uint_as_float(v[e + 2]), 0.f), s.z, t);
+          t = fmaf(fmaxf(__uint_as_float(v[e + 3]), 0.f), s.w, t);
+          acc[c >> 1] = t;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kAEmpty + a]);
+      const int key = kb * kPageTokens + warp * 32 + lane;
+      if (valid && key < shape.nk(r)) {
+        const int t0 = shape.tok0(r) + kTokTile * tt;
+        const int nt = min(kTokTile, shape.ntok(r) - kTokTile * tt);
+        out[(int64_t)t0 * max_keys + key] = acc[0] * ks;
+        if (nt > 1) out[(int64_t)(t0 + 1) * max_keys + key] = acc[1] * ks;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemColsM);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+int g_sms_m[64];
+bool g_attr_m[64];
+
+bool encode_2d_u8(CUtensorMap* map, const void* base, uint64_t rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+  const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Shapes the tensor-core kernel takes: 64 heads, enough query rows for one
+// 128-row box, 16-byte aligned scale arrays (1-D bulk copies).
+// Block and token row coordinates must fit the tensor map's int32 coordinates.
+bool mtp_tc_supported(const uint8_t* q, const float* q_scale, const uint8_t* k, const float* k_scale, int32_t heads,
+                      int32_t num_tokens, int64_t num_blocks) {
+  return heads == kHeadsTc && (int64_t)num_tokens * heads >= 128 && (int64_t)num_tokens * heads < (1ll << 31) &&
+         num_blocks >= 1 && num_blocks * kPageTokens < (1ll << 31) && aligned(q, 16) && aligned(k, 16) &&
+         aligned(q_scale, 16) && aligned(k_scale, 16);
+}
+
+int launch_mtp_tc(const uint8_t* q, const float* q_scale, int32_t num_tokens, const uint8_t* k, const float* k_scale,
+                  int64_t num_blocks, const int32_t* bt, int64_t bt_stride, int32_t max_blocks, const int32_t* num_keys,
+                  const int32_t* cu_tokens, int32_t num_reqs, int32_t max_keys, float* out, int32_t* status,
+                  cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IDX_E_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_encode_mu);
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult qr;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+              cudaSuccess ||
+          qr != cudaDriverEntryPointSuccess || fn == nullptr)
+        return IDX_E_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (!g_attr_m[dev]) {
+      if (cudaFuncSetAttribute(k_mtp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemM) != cudaSuccess ||
+          cudaFuncSetAttribute(k_mtp_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+          cudaDeviceGetAttribute(&g_sms_m[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return IDX_E_CUDA;
+      g_attr_m[dev] = true;
+    }
+  }
+  CUtensorMap kmap, qmap;
+  if (!encode_2d_u8(&kmap, k, (uint64_t)num_blocks * kPageTokens) ||
+      !encode_2d_u8(&qmap, q, (uint64_t)num_tokens * kHeadsTc))
+    return IDX_E_CUDA;
+  ReqShape sh{num_keys, cu_tokens, num_reqs, num_tokens, (int)std::min<int64_t>(max_keys, (int64_t)max_blocks * 128)};
+  // two CTAs per SM: 256 TMEM columns and ~100 KB of shared memory each
+  const int grid = 2 * g_sms_m[dev];
+  k_mtp_tc<<<grid, kThreadsM, kSmemM, stream>>>(kmap, qmap, q_scale, k_scale, num_blocks, bt, bt_stride, sh, max_keys,
+                                                 out, status);
+  return launch_result();
+}
+
+}  // namespace idx

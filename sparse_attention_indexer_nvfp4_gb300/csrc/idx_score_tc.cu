@@ -50,6 +50,7 @@
 // frees its TMEM.
 #include "idx_common.cuh"
 #include "idx_internal.h"
+#include "idx_tc.cuh"
 
 namespace idx {
 namespace {
@@ -73,9 +74,7 @@ constexpr int kMmaM = 128;          // query rows padded to the full datapath
 constexpr int kMmaN = kPageTokens;  // 128 keys
 constexpr uint32_t kAccCols = kMmaN;  // fp32 columns per accumulator
 constexpr uint32_t kTmemCols = 512;   // four accumulators
-// tcgen05 instruction descriptor, kind::f8f6f4: D f32 (bits 4-5 = 1), A and B
-// E4M3 (format 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kMmaM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_f8(kMmaM, kMmaN);
 
 constexpr int kKTile = kPageTokens * kHeadDim;  // 16384
 constexpr int kQTile = kRows * kHeadDim;        // 4096: 32 rows of the A operand
@@ -125,45 +124,6 @@ struct Cursor {
     return entered;
   }
 };
-
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  // K-major, 128-byte swizzle: rows of 128 bytes, 8-row atoms 1,024 bytes apart
-  // (stride byte offset 1024; the leading offset is unused for this layout).
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T (both K-major, 128-byte swizzle).
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// 16 consecutive fp32 columns of this thread's TMEM lane, reduced (max or
-// min) by the load itself; the loaded values are not used.
-#define IDX_TMEM_LDRED16(OP, taddr, red)                                                                 \
-  do {                                                                                                  \
-    uint32_t r_[16];                                                                                    \
-    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x16." OP                                          \
-                 ".f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"           \
-                 : "=r"(r_[0]), "=r"(r_[1]), "=r"(r_[2]), "=r"(r_[3]), "=r"(r_[4]), "=r"(r_[5]),        \
-                   "=r"(r_[6]), "=r"(r_[7]), "=r"(r_[8]), "=r"(r_[9]), "=r"(r_[10]), "=r"(r_[11]),     \
-                   "=r"(r_[12]), "=r"(r_[13]), "=r"(r_[14]), "=r"(r_[15]), "=f"(red)                   \
-                 : "r"(taddr));                                                                         \
-    (void)r_;                                                                                           \
-  } while (0)
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;

@@ -73,3 +73,54 @@ def test_full_size_sampled(lib):
     err = np.abs(o[tokens].astype(np.float64) - ref[tokens].astype(np.float64))
     assert (err <= bound[tokens]).all()
     assert not untouched(o).any()
+
+
+def _ref(wl, tokens=None):
+    return mtp_scores(wl["q"], wl["q_scale"], wl["k"], wl["k_scale"], wl["bt"], wl["num_keys"], wl["cu_tokens"],
+                      wl["max_keys"], tokens=tokens)
+
+
+@pytest.mark.parametrize("heads", [32, 64, 96])
+def test_head_counts(lib, heads):
+    """64 heads take the tensor-core kernel; other head counts the FMA kernel."""
+    wl = W.mtp_workload(seed=50 + heads, num_reqs=3, tokens_per_req=2, heads=heads, num_keys=np.array([640, 129, 300]))
+    out, st = _run(lib, wl)
+    assert st == 0
+    _check(host(out), *_ref(wl))
+
+
+def test_ragged_tokens_and_many_items(lib):
+    """Uneven token counts (0 to 7 per request, so query tiles of one and two
+    tokens and a ring of query buffers that wraps), uneven key counts, more
+    work items than CTAs."""
+    wl = W.mtp_workload(seed=60, num_reqs=40, tokens_per_req=1, heads=64,
+                        num_keys=np.random.default_rng(60).integers(1, 3000, size=40))
+    tok = np.random.default_rng(61).integers(0, 8, size=40)
+    tok[[3, 17]] = 0
+    cu = np.concatenate([[0], np.cumsum(tok)]).astype(np.int32)
+    g = np.random.default_rng(62)
+    wl["cu_tokens"] = cu
+    wl["q"] = W.random_e4m3(W.rng_for(63), (int(cu[-1]), 64, 128))
+    wl["q_scale"] = g.uniform(0.5, 2.0, size=(int(cu[-1]), 64)).astype(np.float32)
+    out, st = _run(lib, wl)
+    assert st == 0
+    _check(host(out), *_ref(wl))
+
+
+def test_out_of_range_block(lib):
+    """A block id outside the pool: its keys stay unwritten and the status says so."""
+    wl = W.mtp_workload(seed=70, num_reqs=3, tokens_per_req=2, heads=64, keys_per_req=640)
+    wl["bt"] = wl["bt"].copy()
+    wl["bt"][1, 2] = wl["num_blocks"] + 5
+    wl["bt"][2, 0] = -1
+    out, st = _run(lib, wl)
+    assert st & 1
+    _check(host(out), *_ref(wl))
+
+
+def test_repeatable(lib):
+    wl = W.mtp_workload(seed=80, num_reqs=8, tokens_per_req=2, heads=64, keys_per_req=8192)
+    first, _ = _run(lib, wl)
+    for _ in range(10):
+        again, _ = _run(lib, wl)
+        assert torch.equal(first.view(torch.int32), again.view(torch.int32))

@@ -81,3 +81,21 @@ def test_paged_gather_and_ragged_keys():
     blk = wl["bt"][0, 1]
     s, _ = mtp_token_scores(wl["q"][1], wl["q_scale"][1], wl["k"][blk, 72:73], wl["k_scale"][blk, 72:73])
     assert out[1, 200] == s[0]
+
+
+def test_out_of_range_block_keys_unwritten():
+    """Keys of a block id outside the pool are not scored; the rest of the
+    request is scored as if the bad block were absent."""
+    wl = W.mtp_workload(seed=6, num_reqs=2, tokens_per_req=1, heads=4, keys_per_req=384)
+    good, _ = mtp_scores(wl["q"], wl["q_scale"], wl["k"], wl["k_scale"], wl["bt"], wl["num_keys"],
+                         wl["cu_tokens"], wl["max_keys"])
+    bt = wl["bt"].copy()
+    bt[0, 1] = wl["num_blocks"]
+    bt[1, 2] = -1
+    out, bound = mtp_scores(wl["q"], wl["q_scale"], wl["k"], wl["k_scale"], bt, wl["num_keys"],
+                            wl["cu_tokens"], wl["max_keys"])
+    assert np.isnan(out[0, 128:256]).all() and (bound[0, 128:256] == 0).all()
+    assert np.isnan(out[1, 256:384]).all()
+    keep = ~np.isnan(out)
+    assert keep.sum() == 2 * 384 - 256
+    assert np.array_equal(out[keep], good[keep])
