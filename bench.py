@@ -53,23 +53,34 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def _kernel_hash() -> str:
+# Sources each kernel is built from (its own file plus the shared headers).
+KERNEL_SOURCES = {
+    "k_score_decode": ["idx_score_tc.cu"],
+    "k_topk_rows": ["idx_topk.cu"],
+    "k_mtp_tc": ["idx_mtp_tc.cu"],
+    "k_dequant_nvfp4": ["idx_dequant.cu"],
+}
+SHARED_SOURCES = ["idx_common.cuh", "idx_tc.cuh", "idx_internal.h", "../../include/idx.h"]
+
+
+def _kernel_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_indexer_nvfp4_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, n), "rb") as f:
-            h.update(n.encode())
+    for n in KERNEL_SOURCES[kernel] + SHARED_SOURCES:
+        with open(os.path.normpath(os.path.join(csrc, n)), "rb") as f:
+            h.update(os.path.basename(n).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def _recorded_traffic(kernel: str):
-    """DRAM bytes per launch recorded from an ncu capture in profiles/traffic.txt,
-    valid only while the kernel sources are unchanged since the capture."""
+    """DRAM bytes per launch recorded from an ncu capture in profiles/traffic.txt
+    (lines "kernel bytes_per_launch source_hash"), valid only while the
+    kernel's sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = _kernel_hash()
+    cur = _kernel_hash(kernel)
     with open(path) as f:
         for line in f:
             parts = line.split("#")[0].split()
@@ -187,6 +198,30 @@ class Timer:
         end.record(self.stream)
         t.cuda.synchronize()
         return start.elapsed_time(end) / iters  # ms
+
+    def run_graph(self, fn, iters: int, per_graph: int = 20) -> float:
+        """Like run(), for sequences of short kernels whose host-side launch
+        cost would otherwise show up as idle gaps: `per_graph` calls of fn are
+        captured into one CUDA graph, which is replayed."""
+        t = self.torch
+        fn()
+        t.cuda.synchronize()
+        g = t.cuda.CUDAGraph()
+        with t.cuda.graph(g):
+            for _ in range(per_graph):
+                fn()
+        g.replay()
+        t.cuda.synchronize()
+        reps = max(1, iters // per_graph)
+        start = t.cuda.Event(enable_timing=True)
+        end = t.cuda.Event(enable_timing=True)
+        stream = t.cuda.current_stream()
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+        t.cuda.synchronize()
+        return start.elapsed_time(end) / (reps * per_graph)  # ms
 
 
 # ---------------------------------------------------------------------------
@@ -323,7 +358,7 @@ def run_native(args, wl, rank: int, world: int, dist):
     assert torch.equal(h_out, out.cpu())
 
     extra = {}
-    if not args.quick and rank == 0:
+    if args.legs and rank == 0:
         extra = secondary(args, torch, idx, W, timer, hbm_peak)
 
     total_scores = units["scores"] * world
@@ -375,62 +410,68 @@ def secondary(args, torch, idx, W, timer, hbm_peak) -> dict:
     def to_dev(x):
         return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
-    # gather/dequant: 256 requests, num_pages U[1,1344], 200,000-page pool
-    g = W.gather_workload(seed=1)
-    kv, bt, npg, off = (to_dev(g[k]) for k in ("kv", "bt", "num_pages", "page_offsets"))
-    out = torch.empty((g["out_pages"], 128, 128), dtype=torch.uint8, device="cuda")
-    fn = lambda: idx.idx_dequant_nvfp4_pages(kv, bt, npg, off, g["max_num_pages"], out)
-    fn()
-    ms = timer.run(fn, iters)
-    byts = g["out_pages"] * (PAGE_BYTES + 16384 + 4)
-    res["gather_dequant"] = {"workload": "256 requests, num_pages U[1,1344], 200,000-page pool, 2% special scales",
-                             "ms": ms, "pages_per_s": g["out_pages"] / (ms / 1e3), "gbs": byts / (ms / 1e3) / 1e9,
-                             "frac_of_hbm": byts / (ms / 1e3) / 1e9 / hbm_peak, "launches": 1}
-    del kv, bt, npg, off, out, g
-    torch.cuda.empty_cache()
+    if "gather" in args.legs:
+        # gather/dequant: 256 requests, num_pages U[1,1344], 200,000-page pool
+        g = W.gather_workload(seed=1)
+        kv, bt, npg, off = (to_dev(g[k]) for k in ("kv", "bt", "num_pages", "page_offsets"))
+        out = torch.empty((g["out_pages"], 128, 128), dtype=torch.uint8, device="cuda")
+        fn = lambda: idx.idx_dequant_nvfp4_pages(kv, bt, npg, off, g["max_num_pages"], out)
+        fn()
+        ms = timer.run(fn, iters)
+        byts = g["out_pages"] * (PAGE_BYTES + 16384 + 4)
+        res["gather_dequant"] = {"workload": "256 requests, num_pages U[1,1344], 200,000-page pool, 2% special scales",
+                                 "ms": ms, "pages_per_s": g["out_pages"] / (ms / 1e3), "gbs": byts / (ms / 1e3) / 1e9,
+                                 "frac_of_hbm": byts / (ms / 1e3) / 1e9 / hbm_peak, "launches": 1}
+        del kv, bt, npg, off, out, g
+        torch.cuda.empty_cache()
 
-    # long context: 16 x 500,000 tokens
-    wl = W.long_context()
-    q, qs, kv, bt, sl = (to_dev(wl[k]) for k in ("q", "q_scale", "kv", "bt", "seq_lens"))
-    scores = torch.empty((16, 32, wl["width"]), dtype=torch.float32, device="cuda")
-    out = torch.empty((16, 8, 4, 16), dtype=torch.int32, device="cuda")
-    wsb = idx.idx_workspace_bytes(16 * 32, wl["width"])
-    ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
-    fn = lambda: idx.idx_decode_step(q, qs, kv, bt, sl, 8, scores, out, ws)
-    fn()
-    ms = timer.run(fn, iters)
-    u = decode_units(wl)
-    res["long_context"] = {"workload": "16 requests x 500,000 tokens (3,906 pages), split rows merged",
-                           "ms": ms, "scores_per_s": u["scores"] / (ms / 1e3),
-                           "index_k_gbs": u["pages"] * PAGE_BYTES / (ms / 1e3) / 1e9,
-                           "frac_of_hbm": u["pages"] * PAGE_BYTES / (ms / 1e3) / 1e9 / hbm_peak,
-                           "launches": 2 + (1 if wsb else 0)}
-    del q, qs, kv, bt, sl, scores, out, ws, wl
-    torch.cuda.empty_cache()
+    if "long" in args.legs:
+        # long context: 16 x 500,000 tokens
+        wl = W.long_context()
+        q, qs, kv, bt, sl = (to_dev(wl[k]) for k in ("q", "q_scale", "kv", "bt", "seq_lens"))
+        scores = torch.empty((16, 32, wl["width"]), dtype=torch.float32, device="cuda")
+        out = torch.empty((16, 8, 4, 16), dtype=torch.int32, device="cuda")
+        wsb = idx.idx_workspace_bytes(16 * 32, wl["width"])
+        ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
+        fn = lambda: idx.idx_decode_step(q, qs, kv, bt, sl, 8, scores, out, ws)
+        fn()
+        ms = timer.run(fn, iters)
+        u = decode_units(wl)
+        res["long_context"] = {"workload": "16 requests x 500,000 tokens (3,906 pages), split rows merged",
+                               "ms": ms, "scores_per_s": u["scores"] / (ms / 1e3),
+                               "index_k_gbs": u["pages"] * PAGE_BYTES / (ms / 1e3) / 1e9,
+                               "frac_of_hbm": u["pages"] * PAGE_BYTES / (ms / 1e3) / 1e9 / hbm_peak,
+                               "launches": 2 + (1 if wsb else 0)}
+        del q, qs, kv, bt, sl, scores, out, ws, wl
+        torch.cuda.empty_cache()
 
-    # multi-token scorer + top-16 per token
-    m = W.mtp_workload(seed=3)
-    args_d = [to_dev(m[k]) for k in ("q", "q_scale", "k", "k_scale", "bt", "num_keys", "cu_tokens")]
-    T = int(m["cu_tokens"][-1])
-    o = torch.empty((T, m["max_keys"]), dtype=torch.float32, device="cuda")
-    idx_out = torch.empty((T, 16), dtype=torch.int32, device="cuda")
-    wsb = idx.idx_workspace_bytes(T, m["max_keys"])
-    ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
+    if "mtp" in args.legs:
+        # multi-token scorer + top-16 per token
+        m = W.mtp_workload(seed=3)
+        args_d = [to_dev(m[k]) for k in ("q", "q_scale", "k", "k_scale", "bt", "num_keys", "cu_tokens")]
+        T = int(m["cu_tokens"][-1])
+        o = torch.empty((T, m["max_keys"]), dtype=torch.float32, device="cuda")
+        idx_out = torch.empty((T, 16), dtype=torch.int32, device="cuda")
+        wsb = idx.idx_workspace_bytes(T, m["max_keys"])
+        ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
 
-    def mtp():
-        idx.idx_mtp_score_fp8(*args_d, m["max_keys"], o)
-        idx.idx_topk16_select(o, idx_out, workspace=ws)
+        def mtp():
+            idx.idx_mtp_score_fp8(*args_d, m["max_keys"], o)
+            idx.idx_topk16_select(o, idx_out, workspace=ws)
 
-    mtp()
-    ms = timer.run(mtp, iters)
-    ms_s = timer.run(lambda: idx.idx_mtp_score_fp8(*args_d, m["max_keys"], o), iters)
-    keys = int(m["num_keys"].sum())
-    flops = 2.0 * T // len(m["num_keys"]) * 64 * 128 * keys
-    kbytes = keys * (128 + 4) + T * (64 * 128 + 64 * 4) + T * m["max_keys"] * 4
-    res["mtp"] = {"workload": "32 requests x 2 tokens x 64 heads, 32,768 keys each; top-16 per token",
-                  "ms": ms, "ms_scorer": ms_s, "token_keys_per_s": T * m["max_keys"] / (ms / 1e3),
-                  "scorer_tflops": flops / (ms_s / 1e3) / 1e12, "scorer_gbs": kbytes / (ms_s / 1e3) / 1e9,
-                  "scorer_frac_of_hbm": kbytes / (ms_s / 1e3) / 1e9 / hbm_peak, "launches": 2 + (1 if wsb else 0)}
+        mtp()
+        ms = timer.run_graph(mtp, max(iters, 100))
+        ms_s = timer.run_graph(lambda: idx.idx_mtp_score_fp8(*args_d, m["max_keys"], o), max(iters, 100))
+        ms_t = timer.run_graph(lambda: idx.idx_topk16_select(o, idx_out, workspace=ws), max(iters, 100))
+        keys = int(m["num_keys"].sum())
+        flops = 2.0 * T // len(m["num_keys"]) * 64 * 128 * keys
+        kbytes = keys * (128 + 4) + T * (64 * 128 + 64 * 4) + T * m["max_keys"] * 4
+        res["mtp"] = {"workload": "32 requests x 2 tokens x 64 heads, 32,768 keys each; top-16 per token",
+                      "ms": ms, "ms_scorer": ms_s, "ms_topk": ms_t, "timing": "CUDA graph of 20 calls, replayed",
+                      "token_keys_per_s": T * m["max_keys"] / (ms / 1e3),
+                      "scorer_tflops": flops / (ms_s / 1e3) / 1e12, "scorer_gbs": kbytes / (ms_s / 1e3) / 1e9,
+                      "scorer_frac_of_hbm": kbytes / (ms_s / 1e3) / 1e9 / hbm_peak, "launches": 2 + (1 if wsb else 0)}
+
     return res
 
 
@@ -441,7 +482,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip secondary workloads; short CPU baseline")
+    ap.add_argument("--legs", default="gather,long,mtp",
+                    help="secondary workloads to time (comma list of gather, long, mtp; empty for none)")
     args = ap.parse_args()
+    args.legs = set() if args.quick else {x for x in args.legs.split(",") if x}
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

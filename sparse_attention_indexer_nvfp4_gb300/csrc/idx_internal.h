@@ -17,24 +17,38 @@ int launch_result();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Columns one warp ranks per pass, and the split of long rows.
-constexpr int kSegCols = 1024;  // 32 columns per lane
-constexpr int kMaxWarpsPerRow = 4;
+// How rows are cut for the top-16 selector.  One warp ranks a segment of
+// 32 * per_lane columns (per_lane of 8, 16, 32, 48 or 64 values in
+// registers); a CTA of 1, 2 or 4 warps covers up to 4 segments of one row
+// (with 1 warp per row, a CTA carries 4 rows); wider rows split across
+// nsplit CTAs whose top-16s are merged through the workspace.
+constexpr int kMaxPerLane = 64;
+constexpr int kWideWarpTarget = 1216;  // 8 warps per SM: below this, halve the segments
 
 struct RowSplit {
-  int warps;   // warps per CTA (1, 2 or 4)
-  int nsplit;  // CTAs per row
+  int per_lane;  // values per lane per segment
+  int warps;     // warps per row in one CTA (1, 2 or 4)
+  int nsplit;    // CTAs per row
 };
 
-inline RowSplit row_split(int32_t width) {
-  const int nseg = width <= 0 ? 1 : (int)((width + kSegCols - 1) / kSegCols);
-  const int warps = nseg <= 1 ? 1 : (nseg <= 2 ? 2 : 4);
-  return RowSplit{warps, (nseg + warps - 1) / warps};
+inline RowSplit row_split(int64_t rows, int32_t width) {
+  const int64_t w = width <= 0 ? 1 : width;
+  if (w <= 32 * kMaxPerLane) {
+    const int need = (int)((w + 31) / 32);
+    const int per_lane = need <= 8 ? 8 : need <= 16 ? 16 : need <= 32 ? 32 : need <= 48 ? 48 : 64;
+    return RowSplit{per_lane, 1, 1};
+  }
+  int per_lane = kMaxPerLane;
+  if (rows * ((w + 32 * per_lane - 1) / (32 * per_lane)) < kWideWarpTarget) per_lane = 32;
+  const int64_t seg = 32 * per_lane;
+  const int nseg = (int)((w + seg - 1) / seg);
+  const int warps = nseg <= 2 ? nseg : 4;
+  return RowSplit{per_lane, warps, (nseg + warps - 1) / warps};
 }
 
 inline size_t topk_workspace_bytes(int32_t rows, int32_t width) {
   if (rows <= 0) return 0;
-  const RowSplit s = row_split(width);
+  const RowSplit s = row_split(rows, width);
   if (s.nsplit <= 1) return 0;
   return (size_t)rows * (size_t)s.nsplit * 16u * sizeof(uint64_t);
 }

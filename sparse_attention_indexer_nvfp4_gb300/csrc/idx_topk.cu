@@ -7,9 +7,16 @@
 // counting the survivors above it, so the result does not depend on slot
 // order; with more than 64 survivors the warp falls back to 16 exact rounds.
 //
-// Long rows: a warp ranks 1,024 columns per pass (32 per lane, in
-// registers).  A CTA of up to 4 warps covers 4,096 columns and merges its
-// warps' top-16s in shared memory; rows wider than that are split across
+// The first pass over a run of scores works on the 32-bit order-preserving
+// image of each score (the upper half of its key) and builds full keys only
+// for survivors: the threshold is the 16th largest lane maximum of those
+// images, so every key of the top 16 still survives (16 lane maxima lie at
+// or above it, each a distinct key at least as large), ties in the image
+// only add survivors.
+//
+// Long rows: a warp ranks a segment of up to 2,048 columns (64 per lane, in
+// registers).  A CTA of up to 4 warps covers 4 segments of one row and
+// merges its warps' top-16s in shared memory; wider rows are split across
 // CTAs whose local top-16s go to the workspace and are merged exactly by a
 // second kernel.  Exactness of both merges is the union argument of
 // "vllm ... indexer_nvfp4_decode_cp" (module docstring): the global top 16
@@ -25,13 +32,28 @@ namespace idx {
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-constexpr int kPerLane = kSegCols / 32;  // 32
+constexpr int kMergePerLane = 32;  // candidates per lane per merge pass
 constexpr int kMaxSurvivors = 64;
+constexpr uint32_t kOrderedPosInf = 0xFF800000u;  // image of +inf (forced columns)
 
 struct WarpScratch {
   uint64_t surv[kMaxSurvivors];
   uint64_t top[kTopK];
 };
+
+// Order-preserving 32-bit image of a score, the upper half of make_key:
+// NaN -> -inf (fmaxf returns the non-NaN operand), -0 -> +0 (adding +0),
+// then the sign-magnitude to unsigned order flip.  Every real score maps
+// to at least image(-inf) = 0x007FFFFF, so 0 is free to mean "no column".
+__device__ __forceinline__ uint32_t ordered_bits(float x) {
+  const float y = fmaxf(x, -INFINITY) + 0.0f;
+  const uint32_t b = __float_as_uint(y);
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t key_from(uint32_t image, int col) {
+  return ((uint64_t)image << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)col);
+}
 
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 #pragma unroll
@@ -42,22 +64,60 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
   return v;
 }
 
-// Bitonic sort of one value per lane across the warp, descending (lane 0 largest).
-__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
+// Bitonic sort of one key per lane across the warp, descending (lane 0 largest).
+__device__ __forceinline__ uint64_t warp_sort_desc_u64(uint64_t v) {
   const uint32_t lane = lane_id();
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
       const uint64_t w = __shfl_xor_sync(kFull, v, j);
-      const bool desc_block = (lane & k) == 0;  // this block sorts descending
-      const bool lower = (lane & j) == 0;
-      const bool keep_max = (lower == desc_block);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
       const uint64_t mx = w > v ? w : v, mn = w > v ? v : w;
       v = keep_max ? mx : mn;
     }
   }
   return v;
+}
+
+// Bitonic sort of one 32-bit value per lane across the warp, descending.
+__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint32_t w = __shfl_xor_sync(kFull, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_max ? max(v, w) : min(v, w);
+    }
+  }
+  return v;
+}
+
+// Rank `count` (<= 64) distinct survivor keys in ws->surv; lanes 0..15 of
+// the result hold the largest 16, descending, 0 padding.
+__device__ __forceinline__ uint64_t rank_survivors(uint32_t count, WarpScratch* ws) {
+  const uint32_t lane = lane_id();
+  const uint64_t a = lane < count ? ws->surv[lane] : 0;
+  const uint64_t b = lane + 32 < count ? ws->surv[lane + 32] : 0;
+  int ra = 0, rb = 0;
+  if (count <= 32) {
+    for (uint32_t j = 0; j < count; ++j) ra += ws->surv[j] > a;
+  } else {
+    for (uint32_t j = 0; j < count; ++j) {
+      const uint64_t v = ws->surv[j];
+      ra += v > a;
+      rb += v > b;
+    }
+  }
+  __syncwarp();
+  if (lane < count && ra < kTopK) ws->top[ra] = a;
+  if (lane + 32 < count && rb < kTopK) ws->top[rb] = b;
+  __syncwarp();
+  const uint64_t result = lane < min(count, (uint32_t)kTopK) ? ws->top[lane] : 0;
+  __syncwarp();
+  return result;
 }
 
 // New running top-16 of (running top-16) U (K keys per lane).  `run` holds the
@@ -70,7 +130,7 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
   uint64_t m = run;
 #pragma unroll
   for (int i = 0; i < K; ++i) m = k[i] > m ? k[i] : m;
-  uint64_t thr = __shfl_sync(kFull, warp_sort_desc(m), 15);
+  uint64_t thr = __shfl_sync(kFull, warp_sort_desc_u64(m), 15);
   if (thr == 0) thr = 1;  // fewer than 16 candidates: every real key survives
 
   uint32_t count = 0;
@@ -85,57 +145,85 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
   for (int i = 0; i < K; ++i) {
     const bool p = k[i] >= thr;
     const uint32_t b = __ballot_sync(kFull, p);
-    const uint32_t pos = count + __popc(b & lt_mask);
-    if (p && pos < kMaxSurvivors) ws->surv[pos] = k[i];
-    count += __popc(b);
+    if (b) {
+      const uint32_t pos = count + __popc(b & lt_mask);
+      if (p && pos < kMaxSurvivors) ws->surv[pos] = k[i];
+      count += __popc(b);
+    }
   }
   __syncwarp();
-  uint64_t result = 0;
-  if (count <= (uint32_t)kMaxSurvivors) {
-    const uint64_t a = lane < count ? ws->surv[lane] : 0;
-    const uint64_t b = lane + 32 < count ? ws->surv[lane + 32] : 0;
-    int ra = 0, rb = 0;
-    for (uint32_t j = 0; j < count; ++j) {
-      const uint64_t v = ws->surv[j];
-      ra += v > a;
-      rb += v > b;
-    }
-    __syncwarp();
-    if (lane < count && ra < kTopK) ws->top[ra] = a;
-    if (lane + 32 < count && rb < kTopK) ws->top[rb] = b;
-    __syncwarp();
-    result = lane < min(count, (uint32_t)kTopK) ? ws->top[lane] : 0;
-  } else {
-    // exact fallback: 16 rounds, each taking the largest key below the last
-    uint64_t prev = ~0ull;
-    for (int r = 0; r < kTopK; ++r) {
-      uint64_t best = run < prev ? run : 0;
+  if (count <= (uint32_t)kMaxSurvivors) return rank_survivors(count, ws);
+  // exact fallback: 16 rounds, each taking the largest key below the last
+  uint64_t result = 0, prev = ~0ull;
+  for (int r = 0; r < kTopK; ++r) {
+    uint64_t best = run < prev ? run : 0;
 #pragma unroll
-      for (int i = 0; i < K; ++i) best = (k[i] < prev && k[i] > best) ? k[i] : best;
-      best = warp_max_u64(best);
-      if ((int)lane == r) result = best;
-      prev = best;
-      if (best == 0) break;
-    }
+    for (int i = 0; i < K; ++i) best = (k[i] < prev && k[i] > best) ? k[i] : best;
+    best = warp_max_u64(best);
+    if ((int)lane == r) result = best;
+    prev = best;
+    if (best == 0) break;
   }
   __syncwarp();
   return result;
 }
 
-// Rank columns [c0, c1) of one fp32 row; running top-16 in `run`.
-__device__ __forceinline__ uint64_t warp_rank_columns(const float* __restrict__ row, int c0, int c1, int fb, int fe,
-                                                      uint64_t run, WarpScratch* ws) {
+// Top-16 keys of columns [c0, c1) of one fp32 row (c1 - c0 <= 32 * K): the
+// 32-bit image pass, keys built only for survivors.  Lanes 0..15 hold the
+// result, descending, 0 padding.
+template <int K, bool kForce>
+__device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws) {
   const uint32_t lane = lane_id();
-  for (int base = c0; base < c1; base += kSegCols) {
-    uint64_t k[kPerLane];
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const int nch = (c1 - c0 + 31) >> 5;
+  uint32_t u[K];
 #pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-      const int col = base + i * 32 + (int)lane;
-      k[i] = col < c1 ? make_key(__ldg(row + col), (uint32_t)col, col >= fb && col < fe) : 0ull;
+  for (int i = 0; i < K; ++i) {
+    const int col = c0 + i * 32 + (int)lane;
+    uint32_t v = 0;
+    if (i < nch && col < c1) {
+      v = ordered_bits(__ldg(row + col));
+      if (kForce && col >= fb && col < fe) v = kOrderedPosInf;
     }
-    run = warp_top16_update(k, run, ws);
+    u[i] = v;
   }
-  return run;
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < K; ++i) m = max(m, u[i]);
+  uint32_t thr = __shfl_sync(kFull, warp_sort_desc_u32(m), 15);
+  if (thr == 0) thr = 1;  // fewer than 16 columns: every one survives
+
+  uint32_t count = 0;
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    if (i < nch) {
+      const bool p = u[i] >= thr;
+      const uint32_t b = __ballot_sync(kFull, p);
+      if (b) {
+        const uint32_t pos = count + __popc(b & lt_mask);
+        if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(u[i], c0 + i * 32 + (int)lane);
+        count += __popc(b);
+      }
+    }
+  }
+  __syncwarp();
+  if (count <= (uint32_t)kMaxSurvivors) return rank_survivors(count, ws);
+  // exact fallback (many equal images): 16 rounds over the full keys
+  uint64_t result = 0, prev = ~0ull;
+  for (int r = 0; r < kTopK; ++r) {
+    uint64_t best = 0;
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      const uint64_t key = u[i] ? key_from(u[i], c0 + i * 32 + (int)lane) : 0ull;
+      best = (key < prev && key > best) ? key : best;
+    }
+    best = warp_max_u64(best);
+    if ((int)lane == r) result = best;
+    prev = best;
+    if (best == 0) break;
+  }
+  __syncwarp();
+  return result;
 }
 
 // Merge the warps' running top-16s (lanes 0..15 of each warp) in warp 0.
@@ -212,23 +300,28 @@ __device__ __forceinline__ void decode_write(const DecodeRows& d, int64_t r, int
   }
 }
 
-// One CTA per (row, split).  Each warp ranks one 1,024-column segment of the
-// split; warp 0 merges.  With nsplit == 1 the CTA writes the final row, else
-// its 16 keys to ws[(row * nsplit + split) * 16].
-template <int kWarps, bool kDecode>
-__global__ void __launch_bounds__(kWarps * 32) k_topk_rows(PlainRows p, DecodeRows d, int nsplit, uint64_t* ws) {
-  __shared__ WarpScratch scratch[kWarps];
-  __shared__ uint64_t cand[kWarps * kTopK];
-  const int64_t r = blockIdx.x;
-  const int split = blockIdx.y;
+// kWarps == 1: a CTA of 4 warps, each ranking one whole row of up to 32 * K
+// columns.  kWarps 2 or 4: one CTA per (row, split), each warp ranking one
+// 32 * K-column segment of the split, warp 0 merging.  With nsplit == 1 the
+// final row is written, else the split's 16 keys go to
+// ws[(row * nsplit + split) * 16].
+template <int kWarps, bool kDecode, int K>
+__global__ void __launch_bounds__(128) k_topk_rows(PlainRows p, DecodeRows d, int64_t rows, int nsplit, uint64_t* ws) {
+  constexpr int kCtaWarps = kWarps == 1 ? 4 : kWarps;
+  constexpr int kSeg = 32 * K;
+  __shared__ WarpScratch scratch[kCtaWarps];
+  __shared__ uint64_t cand[kCtaWarps * kTopK];
   const uint32_t warp = threadIdx.x >> 5;
+  const int64_t r = kWarps == 1 ? (int64_t)blockIdx.x * 4 + warp : (int64_t)blockIdx.x;
+  if (kWarps == 1 && r >= rows) return;
+  const int split = blockIdx.y;
   int n, fb = 0, fe = 0, own = 0;
   const float* row;
   if (kDecode) {
     const DecodeRowInfo info = decode_info(d, r);
     own = info.own;
     if (own + 1 <= kTopK) {  // short row: no ranking
-      if (warp == 0 && split == 0) decode_write(d, r, own, false, 0);
+      if ((kWarps == 1 || warp == 0) && split == 0) decode_write(d, r, own, false, 0);
       return;
     }
     n = info.n;
@@ -239,13 +332,12 @@ __global__ void __launch_bounds__(kWarps * 32) k_topk_rows(PlainRows p, DecodeRo
     fb = p.fb;
     fe = p.fe;
   }
-  const int per_split = kWarps * kSegCols;
-  const int c0 = split * per_split + (int)warp * kSegCols;
-  const int c1 = min(c0 + kSegCols, n);
+  const int c0 = kWarps == 1 ? 0 : (split * kWarps + (int)warp) * kSeg;
+  const int c1 = min(c0 + kSeg, n);
   uint64_t run = 0;
-  if (c0 < c1) run = warp_rank_columns(row, c0, c1, fb, fe, 0ull, &scratch[warp]);
+  if (c0 < c1) run = warp_top16_seg<K, !kDecode>(row, c0, c1, fb, fe, &scratch[warp]);
   run = cta_merge<kWarps>(run, cand, &scratch[0]);
-  if (warp != 0) return;
+  if (kWarps > 1 && warp != 0) return;
   if (nsplit == 1) {
     if (kDecode)
       decode_write(d, r, own, true, run);
@@ -272,10 +364,10 @@ __global__ void __launch_bounds__(128) k_topk_merge(PlainRows p, DecodeRows d, i
   const uint64_t* cand = ws + r * (int64_t)nsplit * kTopK;
   const int total = nsplit * kTopK;
   uint64_t run = 0;
-  for (int base = 0; base < total; base += kSegCols) {
-    uint64_t k[kPerLane];
+  for (int base = 0; base < total; base += 32 * kMergePerLane) {
+    uint64_t k[kMergePerLane];
 #pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
+    for (int i = 0; i < kMergePerLane; ++i) {
       const int j = base + i * 32 + (int)lane;
       k[i] = j < total ? cand[j] : 0ull;
     }
@@ -287,18 +379,37 @@ __global__ void __launch_bounds__(128) k_topk_merge(PlainRows p, DecodeRows d, i
     plain_write(p, r, run);
 }
 
+template <bool kDecode, int kWarps, int K>
+void launch_k(const PlainRows& p, const DecodeRows& d, int64_t rows, int nsplit, uint64_t* ws, cudaStream_t s) {
+  const dim3 grid(kWarps == 1 ? (unsigned)((rows + 3) / 4) : (unsigned)rows, (unsigned)nsplit);
+  k_topk_rows<kWarps, kDecode, K><<<grid, (kWarps == 1 ? 4 : kWarps) * 32, 0, s>>>(p, d, rows, nsplit, ws);
+}
+
 template <bool kDecode>
 int launch_rows(const PlainRows& p, const DecodeRows& d, int64_t rows, int32_t width, void* ws, cudaStream_t s) {
-  const RowSplit sp = row_split(width);
+  const RowSplit sp = row_split(rows, width);
   if (sp.nsplit > 65535) return IDX_E_TOO_LARGE;
   if (rows > 0x7FFFFFFFLL) return IDX_E_TOO_LARGE;
   uint64_t* wsk = static_cast<uint64_t*>(ws);
   if (sp.nsplit > 1 && wsk == nullptr) return IDX_E_WORKSPACE;
-  const dim3 grid((unsigned)rows, (unsigned)sp.nsplit);
-  switch (sp.warps) {
-    case 1: k_topk_rows<1, kDecode><<<grid, 32, 0, s>>>(p, d, sp.nsplit, wsk); break;
-    case 2: k_topk_rows<2, kDecode><<<grid, 64, 0, s>>>(p, d, sp.nsplit, wsk); break;
-    default: k_topk_rows<4, kDecode><<<grid, 128, 0, s>>>(p, d, sp.nsplit, wsk); break;
+  if (sp.warps == 1) {
+    switch (sp.per_lane) {
+      case 8: launch_k<kDecode, 1, 8>(p, d, rows, 1, wsk, s); break;
+      case 16: launch_k<kDecode, 1, 16>(p, d, rows, 1, wsk, s); break;
+      case 32: launch_k<kDecode, 1, 32>(p, d, rows, 1, wsk, s); break;
+      case 48: launch_k<kDecode, 1, 48>(p, d, rows, 1, wsk, s); break;
+      default: launch_k<kDecode, 1, 64>(p, d, rows, 1, wsk, s); break;
+    }
+  } else if (sp.warps == 2) {
+    if (sp.per_lane == 32)
+      launch_k<kDecode, 2, 32>(p, d, rows, sp.nsplit, wsk, s);
+    else
+      launch_k<kDecode, 2, 64>(p, d, rows, sp.nsplit, wsk, s);
+  } else {
+    if (sp.per_lane == 32)
+      launch_k<kDecode, 4, 32>(p, d, rows, sp.nsplit, wsk, s);
+    else
+      launch_k<kDecode, 4, 64>(p, d, rows, sp.nsplit, wsk, s);
   }
   int rc = launch_result();
   if (rc != IDX_OK || sp.nsplit == 1) return rc;

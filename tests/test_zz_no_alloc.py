@@ -53,7 +53,7 @@ def test_no_alloc_matches_workspace_entry_on_two_calls_in_a_row(lib):
 
 
 def test_no_alloc_rejects_rows_beyond_its_scratch(lib):
-    rows, width = 4096, 40000
+    rows, width = 32768, 9000  # 2 CTAs per row: 8 MiB of split-row scratch
     need = lib.idx_workspace_bytes(rows, width)
     assert need > lib.NOALLOC_SCRATCH_BYTES
     scores = torch.zeros((rows, width), dtype=torch.float32, device="cuda")
