@@ -60,7 +60,7 @@ KERNEL_SOURCES = {
     "k_mtp_tc": ["idx_mtp_tc.cu"],
     "k_dequant_nvfp4": ["idx_dequant.cu"],
 }
-SHARED_SOURCES = ["idx_common.cuh", "idx_tc.cuh", "idx_internal.h", "../../include/idx.h"]
+SHARED_SOURCES = ["idx_common.cuh", "idx_tc.cuh", "../../include/idx.h"]  # device code the kernels include
 
 
 def _kernel_hash(kernel: str) -> str:
