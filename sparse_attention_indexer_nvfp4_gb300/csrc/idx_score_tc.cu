@@ -12,7 +12,8 @@
 //
 //   producer (1 warp)   raw NVFP4 page -> 8-stage shared-memory ring, one
 //                       9,216-byte bulk copy per page (a 72-byte row is not a
-//                       legal TMA box); its lanes fetch block ids 32 pages ahead;
+//                       legal TMA box); lane s refills stage s, so the eight
+//                       stages are refilled in parallel;
 //   dequant (16 warps)  4 groups of 4 warps, group g takes pages i = g (mod 4)
 //                       and owns two K tiles (one filled while the MMA reads
 //                       the other): the page becomes a 128B-swizzled
@@ -93,6 +94,7 @@ constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
 static_assert(kOffQ + (kQBufs - 1) * kQTile + kMmaM * kHeadDim <= kOffRaw, "A rows 32-127 stay inside the CTA's tiles");
 static_assert(kStages % kGroups == 0, "raw stage s is consumed by group s % kGroups only");
+static_assert(kStages <= 32, "one producer lane per raw stage");
 
 struct Misc {
   uint32_t tmem_base;
@@ -272,52 +274,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
 
   if (warp == kProducerWarp) {
     // ---------------- producer: raw pages into the ring ----------------
-    Cursor lc;  // lane k walks pages k, k + 32, k + 64, ...
+    // Lane s < kStages owns ring stage s and fills it with pages i = s (mod
+    // kStages): the stages are refilled in parallel, one wait and one bulk
+    // copy per lane per round, instead of one serial wait + copy chain per
+    // page (each mbarrier operation costs the issuing thread ~100+ cycles).
+    // Block ids are loaded one round ahead.
+    const bool owner = lane < kStages;
+    Cursor lc;
     lc.init(seq_lens, num_reqs, cap, b0, j0);
-    lc.advance(lane);
-    int issued = 0;
-    int64_t ids = lane < count ? (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j] : -1;
-    lc.advance(32);
-    bool ok_all = true;
-    for (int base = 0; base < count && ok_all; base += 32) {
-      int64_t ids_next = -1;
-      if (base + 32 < count) {
-        ids_next = base + 32 + lane < count ? (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j] : -1;
-        lc.advance(32);
+    if (owner) lc.advance(lane);
+    int64_t blk = (owner && lane < count) ? (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j] : -1;
+    int last = -1;  // the last page this lane issued into its stage
+    for (int base = 0; base < count; base += kStages) {
+      const int i = base + lane;
+      const bool active = owner && i < count;
+      int64_t blk_next = -1;
+      if (active && i + kStages < count) {
+        lc.advance(kStages);
+        blk_next = (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j];
       }
-      const int n = min(32, count - base);
-      for (int k = 0; k < n; ++k) {
-        const int i = base + k;
-        const int64_t blk = __shfl_sync(0xFFFFFFFFu, ids, k);
-        int ok = 1;
-        if (lane == 0) {
-          const int stage = i % kStages;
-          if (timed_wait(&bars[kRawEmpty + stage], ((uint32_t)(i / kStages) & 1u) ^ 1u, misc, status)) {
-            const bool valid = blk >= 0 && blk < num_blocks;
-            valid_ring[i % kRing] = valid ? 1 : 0;
-            if (valid) {
-              mbar_arrive_expect_tx(&bars[kRawFull + stage], kPageBytes);
-              bulk_g2s(smem + kOffRaw + stage * kPageBytes, kv + blk * kPageBytes, kPageBytes,
-                       &bars[kRawFull + stage]);
-            } else {
-              mbar_arrive(&bars[kRawFull + stage]);
-            }
-            issued = i + 1;
+      bool ok = true;
+      if (active) {
+        ok = timed_wait(&bars[kRawEmpty + lane], ((uint32_t)(i / kStages) & 1u) ^ 1u, misc, status);
+        if (ok) {
+          const bool valid = blk >= 0 && blk < num_blocks;
+          valid_ring[i % kRing] = valid ? 1 : 0;
+          if (valid) {
+            mbar_arrive_expect_tx(&bars[kRawFull + lane], kPageBytes);
+            bulk_g2s(smem + kOffRaw + lane * kPageBytes, kv + blk * kPageBytes, kPageBytes, &bars[kRawFull + lane]);
           } else {
-            ok = 0;
+            mbar_arrive(&bars[kRawFull + lane]);
           }
-        }
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
-          ok_all = false;
-          break;
+          last = i;
         }
       }
-      ids = ids_next;
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      blk = blk_next;
     }
     // never leave with a copy in flight
-    if (lane == 0)
-      for (int i = max(0, issued - kStages); i < issued; ++i)
-        mbar_wait(&bars[kRawFull + i % kStages], (uint32_t)(i / kStages) & 1u, nullptr);
+    if (last >= 0) mbar_wait(&bars[kRawFull + lane], (uint32_t)(last / kStages) & 1u, nullptr);
   } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kIssuers) {
     // ---------------- MMA issuers ----------------
     const int e = warp - kIssuerWarp0;
@@ -368,7 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
         neg = __any_sync(0xFFFFFFFFu, !(qs >= 0.f));
         own = iq >= 0 ? floor_div_page(seq_lens[b] - query_len + iq) : -1;
       }
-      if (!timed_wait(&bars[kAccFull + e], (uint32_t)(i / kPipe) & 1u, misc, status)) break;
+      const bool ready = timed_wait(&bars[kAccFull + e], (uint32_t)(i / kPipe) & 1u, misc, status);
+      if (!__all_sync(0xFFFFFFFFu, ready)) break;  // the TMEM loads below are warp-wide
       tc_fence_after();
       if (lane == 0) done_ring[i % kRing] = i + 1;  // page i's MMA is complete
       const bool page_ok = valid_ring[i % kRing] != 0;
