@@ -23,14 +23,15 @@
 //                       so it is the same function; 8 copies to spread a
 //                       half-warp's reads over the banks), 9 operations per 8
 //                       elements;
-//   MMA (2 warps)       issuer e takes pages i = e (mod 2); it waits for the
+//   MMA (4 warps)       issuer e takes pages i = e (mod 4); it waits for the
 //                       page's K tile (its 4 dequant warps) and for its
 //                       accumulator (the epilogue of page i - 4), then issues tcgen05.mma
 //                       kind::f8f6f4, M=128 x N=128 (keys) x K=128 (four K=32
 //                       steps) into TMEM accumulator i % 4.  MMA issue holds
-//                       its thread until the tensor core accepts the work, so
-//                       one issuer's barrier waits would idle the tensor core;
-//                       two issuers hide each other's waits;
+//                       its thread until the tensor core accepts the work, and
+//                       each mbarrier wait or commit costs the thread ~100-200
+//                       cycles, so one issuer's waits would idle the tensor
+//                       core; four issuers hide each other's waits;
 //   epilogue (4 warps)  warp e takes pages i = e (mod 4) and accumulator e,
 //                       reduces each (slot, head) row's 128 key scores with
 //                       tcgen05.ld.red (the load takes the max), applies q_scale
@@ -62,11 +63,11 @@ constexpr int kGroupTiles = 2;  // K tiles per group: the group fills one while 
 constexpr int kKTiles = kGroups * kGroupTiles;
 constexpr int kGroupWarps = 4;  // each warp of a group takes a quarter page (32 keys)
 constexpr int kPipe = 4;        // accumulators and epilogue warps
-constexpr int kIssuers = 2;     // MMA issuing warps
+constexpr int kIssuers = 4;     // MMA issuing warps; issuer e owns accumulator e
 constexpr int kQBufs = 2;       // query tiles in shared memory (request k uses k % 2)
-constexpr int kProducerWarp = 22;
+constexpr int kProducerWarp = 24;
 constexpr int kIssuerWarp0 = 20;
-constexpr int kThreads = 23 * 32;
+constexpr int kThreads = 25 * 32;
 __host__ __device__ constexpr bool is_epi_warp(int w) { return w < 16 && (w & 3) == 0; }
 // dequant warp index 0..15 of warp w (w in 1-3, 5-7, 9-11, 13-15, 16-19)
 __device__ __forceinline__ int worker_index(int w) { return w < 16 ? w - (w >> 2) - 1 : w - 4; }
@@ -95,6 +96,7 @@ constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base t
 static_assert(kOffQ + (kQBufs - 1) * kQTile + kMmaM * kHeadDim <= kOffRaw, "A rows 32-127 stay inside the CTA's tiles");
 static_assert(kStages % kGroups == 0, "raw stage s is consumed by group s % kGroups only");
 static_assert(kStages <= 32, "one producer lane per raw stage");
+static_assert(kIssuers == kPipe, "issuer e is the only waiter of accumulator e's empty barrier");
 
 struct Misc {
   uint32_t tmem_base;
@@ -150,8 +152,7 @@ __device__ __forceinline__ uint2 dq8_lut(uint32_t w, uint32_t lo, uint32_t hi) {
 
 // mbarrier arrive issued after `after` is computed (an input of the asm).
 __device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, uint32_t after) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar)), "r"(after)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)), "r"(after) : "memory");
 }
 
 __device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, Misc* misc, int32_t* status) {
@@ -324,8 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       for (int i = e; i < count; i += kIssuers) {
         const int s = i % kPipe;
         const int tile = (i % kGroups) * kGroupTiles + (i / kGroups) % kGroupTiles;
-        if (!spin_wait(&bars[kKtFull + tile], (uint32_t)(i / kKTiles) & 1u, misc, status)) break;
-        if (!spin_wait(&bars[kAccEmpty + s], ((uint32_t)(i / kPipe) & 1u) ^ 1u, misc, status)) break;
+        const uint32_t p_kt = (uint32_t)(i / kKTiles) & 1u, p_acc = ((uint32_t)(i / kPipe) & 1u) ^ 1u;
+        bool kt_ok, acc_ok;
+        mbar_test2(&bars[kKtFull + tile], p_kt, &bars[kAccEmpty + s], p_acc, kt_ok, acc_ok);
+        if (!kt_ok && !timed_wait(&bars[kKtFull + tile], p_kt, misc, status)) break;
+        if (!acc_ok && !timed_wait(&bars[kAccEmpty + s], p_acc, misc, status)) break;
         tc_fence_after();
         const uint64_t adesc = sw128_desc(sbase + kOffQ + (uint32_t)(req_ord % kQBufs) * kQTile);
         const uint64_t bdesc = sw128_desc(sbase + kOffK + (uint32_t)tile * kKTile);
@@ -368,21 +372,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       tc_fence_after();
       if (lane == 0) done_ring[i % kRing] = i + 1;  // page i's MMA is complete
       const bool page_ok = valid_ring[i % kRing] != 0;
+      // two reductions in flight per wait (each holds 16 registers of loaded values)
       float mx = -INFINITY, mn = INFINITY;
 #pragma unroll
-      for (int c = 0; c < (int)kAccCols; c += 16) {
-        float r0;
+      for (int c = 0; c < (int)kAccCols; c += 32) {
+        float r0, r1;
         IDX_TMEM_LDRED16("max", acc + (uint32_t)c, r0);
+        IDX_TMEM_LDRED16("max", acc + (uint32_t)(c + 16), r1);
         tmem_wait_ld();
-        mx = fmaxf(mx, r0);
+        mx = fmaxf(mx, fmaxf(r0, r1));
       }
       if (neg) {
 #pragma unroll
-        for (int c = 0; c < (int)kAccCols; c += 16) {
-          float r0;
+        for (int c = 0; c < (int)kAccCols; c += 32) {
+          float r0, r1;
           IDX_TMEM_LDRED16("min", acc + (uint32_t)c, r0);
+          IDX_TMEM_LDRED16("min", acc + (uint32_t)(c + 16), r1);
           tmem_wait_ld();
-          mn = fminf(mn, r0);
+          mn = fminf(mn, fminf(r0, r1));
         }
       }
       tc_fence_before();
@@ -415,10 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       const bool first_of_request = b != prev_b;
       prev_b = b;
       const int stage = i % kStages;
-      if (!timed_wait(&bars[kRawFull + stage], (uint32_t)(i / kStages) & 1u, misc, status)) break;
       const int tile = grp * kGroupTiles + (i / kGroups) % kGroupTiles;  // used by pages i, i + 8, ... of this group
       uint8_t* kd = smem + kOffK + tile * kKTile;
-      if (!timed_wait(&bars[kKtEmpty + tile], ((uint32_t)(i / (kGroups * kGroupTiles)) & 1u) ^ 1u, misc, status)) break;
+      {
+        const uint32_t p_raw = (uint32_t)(i / kStages) & 1u;
+        const uint32_t p_kt = ((uint32_t)(i / (kGroups * kGroupTiles)) & 1u) ^ 1u;
+        bool raw_ok, kt_ok;
+        mbar_test2(&bars[kRawFull + stage], p_raw, &bars[kKtEmpty + tile], p_kt, raw_ok, kt_ok);
+        if (!raw_ok) raw_ok = timed_wait(&bars[kRawFull + stage], p_raw, misc, status);
+        if (raw_ok && !kt_ok) kt_ok = timed_wait(&bars[kKtEmpty + tile], p_kt, misc, status);
+        if (!__all_sync(0xFFFFFFFFu, raw_ok && kt_ok)) break;  // the warp stays converged for its ballot
+      }
       if (first_of_request && wg == 0) {
         // The request's 32 query rows into query buffer req_ord % 2.  Request
         // req_ord - 2 used that buffer; its pages are < the first page of
