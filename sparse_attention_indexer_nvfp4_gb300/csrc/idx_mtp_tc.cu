@@ -11,17 +11,20 @@
 //
 // Work items are (request, token pair, 128-key block) in that order; one
 // persistent CTA (two per SM) takes a contiguous slice.  Roles:
-//   producer (warp 4)  TMA: the key block [128 keys, 128 B] and the token
-//                      pair's query rows [128, 128 B] with 128-byte swizzle
-//                      straight into the layout the tensor core reads, plus
-//                      k_scale and q_scale by 1-D bulk copies;
-//   MMA (warp 5)       one tcgen05.mma group (4 x K=32) per item into one of
-//                      two 128-column accumulators;
-//   epilogue (warps 0-3) warp w owns keys 32w..32w+31 (TMEM lane quarter w).
-// Every barrier's phases are consumed in order by each role that waits on it;
-// the epilogue also waits on the (already complete) copy barriers of the
-// tiles it reads scales from, which cannot run two phases ahead of it
-// because it releases those buffers itself.
+//   producer (warp 8)  TMA, in item order from lane 0 (the warp's lanes load
+//                      block ids 32 items ahead): the key block [128 keys,
+//                      128 B] and the token pair's query rows [128, 128 B]
+//                      with 128-byte swizzle straight into the layout the
+//                      tensor core reads, plus k_scale by a 1-D bulk copy;
+//   MMA (warp 9)       one tcgen05.mma group (4 x K=32) per item into one of
+//                      two 128-column accumulators (item i -> i % 2);
+//   epilogue (warps 0-7) set a = warps 4a..4a+3 drains accumulator a; warp w
+//                      owns keys 32 (w % 4) .. + 31 (TMEM lane quarter w % 4)
+//                      and reads q_scale through L1 (one address per warp).
+// Every barrier's phases are consumed in order by each role that waits on it.
+// The key tiles go back to the producer as soon as the MMA has read them;
+// k_scale and the validity flag travel in a separate, deeper ring that the
+// epilogue releases.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -35,26 +38,27 @@ namespace {
 
 constexpr int kHeadsTc = 64;
 constexpr int kTokTile = 2;                  // tokens per MMA (N = 2 x 64 = 128)
-constexpr int kStages = 4;                   // key-block ring
+constexpr int kStages = 4;                   // key-block ring (released by the MMA alone)
+constexpr int kKsSlots = 16;                 // k_scale ring (released by the epilogue)
 constexpr int kQBufsM = 2;                   // query tiles (one per token pair in flight)
 constexpr int kKTileBytes = kPageTokens * kHeadDim;   // 16384
 constexpr int kQTileBytes = kTokTile * kHeadsTc * kHeadDim;  // 16384
 constexpr int kKsBytes = kPageTokens * 4;    // 512
-constexpr int kQsBytes = kTokTile * kHeadsTc * 4;  // 512
-constexpr int kRingM = 32;
-constexpr int kThreadsM = 6 * 32;
-constexpr int kProdWarp = 4, kMmaWarpM = 5;
+constexpr int kRingM = kKsSlots;  // validity flags travel with the k_scale slots
+constexpr int kThreadsM = 10 * 32;
+constexpr int kEpiSets = 2;  // epilogue warp sets: set a (warps 4a..4a+3) drains accumulator a
+constexpr int kProdWarp = 8, kMmaWarpM = 9;
 constexpr uint32_t kAccColsM = 128, kTmemColsM = 256;
 constexpr uint32_t kIdescM = idesc_f8(128, kTokTile * kHeadsTc);
 
 constexpr int kOffKm = 0;
 constexpr int kOffQm = kOffKm + kStages * kKTileBytes;
 constexpr int kOffKs = kOffQm + kQBufsM * kQTileBytes;
-constexpr int kOffQs = kOffKs + kStages * kKsBytes;
-constexpr int kOffValidM = kOffQs + kQBufsM * kQsBytes;
+constexpr int kOffValidM = kOffKs + kKsSlots * kKsBytes;
 constexpr int kOffBarM = kOffValidM + kRingM * 4;
 enum BarsM { kKFull = 0, kKEmpty = kStages, kQFull = 2 * kStages, kQEmpty = kQFull + kQBufsM,
-             kAFull = kQEmpty + kQBufsM, kAEmpty = kAFull + 2, kDrainM = kAEmpty + 2, kNumBarsM };
+             kAFull = kQEmpty + kQBufsM, kAEmpty = kAFull + 2, kKsFull = kAEmpty + 2, kKsEmpty = kKsFull + kKsSlots,
+             kDrainM = kKsEmpty + kKsSlots, kNumBarsM };
 constexpr int kOffMiscM = kOffBarM + kNumBarsM * 8;
 constexpr int kSmemM = kOffMiscM + 64 + 1024;
 
@@ -104,7 +108,7 @@ struct ItemCursor {
   }
 };
 
-__global__ void __launch_bounds__(kThreadsM) k_mtp_tc(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__ CUtensorMap kmap,
                                                       const __grid_constant__ CUtensorMap qmap,
                                                       const float* __restrict__ q_scale,
                                                       const float* __restrict__ k_scale, int64_t num_blocks,
@@ -162,15 +166,19 @@ __global__ void __launch_bounds__(kThreadsM) k_mtp_tc(const __grid_constant__ CU
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[kKFull + s], 1);
-      mbar_init(&bars[kKEmpty + s], 1 + 4);  // the MMA (commit) and the 4 epilogue warps (k_scale read)
+      mbar_init(&bars[kKEmpty + s], 1);  // the MMA's commit
+    }
+    for (int s = 0; s < kKsSlots; ++s) {
+      mbar_init(&bars[kKsFull + s], 1);
+      mbar_init(&bars[kKsEmpty + s], 4);  // the item's 4 epilogue warps read k_scale and the flag
     }
     for (int s = 0; s < kQBufsM; ++s) {
       mbar_init(&bars[kQFull + s], 1);
-      mbar_init(&bars[kQEmpty + s], 1 + 4);  // the MMA leaving the tile and the 4 epilogue warps
+      mbar_init(&bars[kQEmpty + s], 1);  // the MMA leaving the tile
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kAFull + s], 1);
-      mbar_init(&bars[kAEmpty + s], 4);
+      mbar_init(&bars[kAEmpty + s], 4);  // epilogue set s
     }
     mbar_init(&bars[kDrainM], 1);
     fence_mbar_init();
@@ -183,43 +191,80 @@ __global__ void __launch_bounds__(kThreadsM) k_mtp_tc(const __grid_constant__ CU
   const int r0 = misc->r0, rem0 = misc->rem0;
 
   if (warp == kProdWarp) {
-    if (lane == 0) {
-      ItemCursor cur;
-      cur.init(shape, r0, rem0);
-      int qord = -1, pr = -1, ptt = -1, issued = 0;  // qord: query tiles issued - 1
-      for (int i = 0; i < count; ++i) {
-        if (cur.r != pr || cur.tt != ptt) {
-          const int qb = (qord + 1) % kQBufsM;
-          if (!timed_wait_flag(&bars[kQEmpty + qb], ((uint32_t)((qord + 1) / kQBufsM) & 1u) ^ 1u, abort_flag, status))
-            break;
-          pr = cur.r, ptt = cur.tt;
-          ++qord;
-          const int t0 = shape.tok0(cur.r) + kTokTile * cur.tt;
-          const int nt = min(kTokTile, shape.ntok(cur.r) - kTokTile * cur.tt);
-          mbar_arrive_expect_tx(&bars[kQFull + qb], kQTileBytes + nt * kHeadsTc * 4);
-          tma_load_2d(smem + kOffQm + qb * kQTileBytes, &qmap, 0, t0 * kHeadsTc, &bars[kQFull + qb]);
-          bulk_g2s(smem + kOffQs + qb * kQsBytes, q_scale + (int64_t)t0 * kHeadsTc, nt * kHeadsTc * 4,
-                   &bars[kQFull + qb]);
-        }
-        const int stage = i % kStages;
-        if (!timed_wait_flag(&bars[kKEmpty + stage], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort_flag, status)) break;
-        const int64_t blk = bt[(int64_t)cur.r * bt_stride + cur.kb];
-        const bool valid = blk >= 0 && blk < num_blocks;
-        valid_ring[i % kRingM] = valid ? 1 : 0;
-        if (valid) {
-          mbar_arrive_expect_tx(&bars[kKFull + stage], kKTileBytes + kKsBytes);
-          tma_load_2d(smem + kOffKm + stage * kKTileBytes, &kmap, 0, (int)(blk * kPageTokens), &bars[kKFull + stage]);
-          bulk_g2s(smem + kOffKs + stage * kKsBytes, k_scale + blk * kPageTokens, kKsBytes, &bars[kKFull + stage]);
-        } else {
-          report(status, IDX_ST_BLOCK_OOR);
-          mbar_arrive(&bars[kKFull + stage]);
-        }
-        issued = i + 1;
-        cur.next();
+    // Lane 0 issues the copies in item order; the warp's lanes load the next
+    // 32 items' block ids together, one chunk ahead, so no block-table load
+    // sits on lane 0's per-item chain.
+    ItemCursor cur;
+    cur.init(shape, r0, rem0);
+    ItemCursor pf;  // lane l: item base + l
+    pf.init(shape, r0, rem0);
+    for (int k = 0; k < lane && k < count; ++k) pf.next();
+    int64_t blk_l = lane < count ? (int64_t)bt[(int64_t)pf.r * bt_stride + pf.kb] : -1;
+    int qord = -1, pr = -1, ptt = -1, issued = 0;  // qord: query tiles issued - 1
+    bool ok_all = true;
+    for (int base = 0; base < count && ok_all; base += 32) {
+      int64_t blk_next = -1;
+      if (base + 32 + lane < count) {
+        for (int k = 0; k < 32; ++k) pf.next();
+        blk_next = (int64_t)bt[(int64_t)pf.r * bt_stride + pf.kb];
       }
-      // never leave with a copy in flight: the last uses of every stage and query buffer
+      const int n = min(32, count - base);
+      for (int k = 0; k < n; ++k) {
+        const int i = base + k;
+        const int64_t blk = __shfl_sync(0xFFFFFFFFu, blk_l, k);
+        int ok = 1;
+        if (lane == 0) {
+          if (cur.r != pr || cur.tt != ptt) {
+            const int qb = (qord + 1) % kQBufsM;
+            if (timed_wait_flag(&bars[kQEmpty + qb], ((uint32_t)((qord + 1) / kQBufsM) & 1u) ^ 1u, abort_flag, status)) {
+              pr = cur.r, ptt = cur.tt;
+              ++qord;
+              const int t0 = shape.tok0(cur.r) + kTokTile * cur.tt;
+              mbar_arrive_expect_tx(&bars[kQFull + qb], kQTileBytes);
+              tma_load_2d(smem + kOffQm + qb * kQTileBytes, &qmap, 0, t0 * kHeadsTc, &bars[kQFull + qb]);
+            } else {
+              ok = 0;
+            }
+          }
+          const int stage = i % kStages, ks = i % kKsSlots;
+          const uint32_t p_k = ((uint32_t)(i / kStages) & 1u) ^ 1u, p_ks = ((uint32_t)(i / kKsSlots) & 1u) ^ 1u;
+          bool k_free = false, ks_free = false;
+          if (ok) {
+            mbar_test2(&bars[kKEmpty + stage], p_k, &bars[kKsEmpty + ks], p_ks, k_free, ks_free);
+            if (!k_free) k_free = timed_wait_flag(&bars[kKEmpty + stage], p_k, abort_flag, status);
+            if (k_free && !ks_free) ks_free = timed_wait_flag(&bars[kKsEmpty + ks], p_ks, abort_flag, status);
+            ok = k_free && ks_free;
+          }
+          if (ok) {
+            const bool valid = blk >= 0 && blk < num_blocks;
+            valid_ring[ks] = valid ? 1 : 0;
+            if (valid) {
+              mbar_arrive_expect_tx(&bars[kKFull + stage], kKTileBytes);
+              tma_load_2d(smem + kOffKm + stage * kKTileBytes, &kmap, 0, (int)(blk * kPageTokens), &bars[kKFull + stage]);
+              mbar_arrive_expect_tx(&bars[kKsFull + ks], kKsBytes);
+              bulk_g2s(smem + kOffKs + ks * kKsBytes, k_scale + blk * kPageTokens, kKsBytes, &bars[kKsFull + ks]);
+            } else {
+              report(status, IDX_ST_BLOCK_OOR);
+              mbar_arrive(&bars[kKFull + stage]);
+              mbar_arrive(&bars[kKsFull + ks]);
+            }
+            issued = i + 1;
+          }
+          cur.next();
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+          ok_all = false;
+          break;
+        }
+      }
+      blk_l = blk_next;
+    }
+    if (lane == 0) {
+      // never leave with a copy in flight: the last uses of every stage, k_scale slot and query buffer
       for (int i = max(0, issued - kStages); i < issued; ++i)
         mbar_wait(&bars[kKFull + i % kStages], (uint32_t)(i / kStages) & 1u, nullptr);
+      for (int i = max(0, issued - kKsSlots); i < issued; ++i)
+        mbar_wait(&bars[kKsFull + i % kKsSlots], (uint32_t)(i / kKsSlots) & 1u, nullptr);
       for (int qo = max(0, qord - kQBufsM + 1); qo <= qord; ++qo)
         mbar_wait(&bars[kQFull + qo % kQBufsM], (uint32_t)(qo / kQBufsM) & 1u, nullptr);
     }
@@ -255,63 +300,65 @@ __global__ void __launch_bounds__(kThreadsM) k_mtp_tc(const __grid_constant__ CU
         mbar_wait(&bars[kDrainM], 0, nullptr);
       }
     }
-  } else if (warp < 4) {
-    // epilogue: warp w owns keys 32w + lane of each block (TMEM lane quarter w)
+  } else if (warp < 4 * kEpiSets) {
+    // epilogue: set a = warp / 4 takes items i = a (mod 2) (accumulator a);
+    // warp w owns keys 32 (w % 4) + lane of each block (TMEM lane quarter w % 4)
+    const int set = warp >> 2, quarter = warp & 3;
     ItemCursor cur;
     cur.init(shape, r0, rem0);
-    int qord = -1, pr = -1, ptt = -1;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    for (int i = 0; i < count; ++i) {
+    if (set == 1 && count > 1) cur.next();
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t acc_addr = tmem + lane_base + (uint32_t)set * kAccColsM;
+    for (int i = set; i < count; i += kEpiSets) {
       const int r = cur.r, tt = cur.tt, kb = cur.kb;
       cur.next();
-      if (r != pr || tt != ptt) {
-        pr = r, ptt = tt;
-        __syncwarp();
-        if (qord >= 0 && lane == 0) mbar_arrive(&bars[kQEmpty + qord % kQBufsM]);  // done with its q_scale
-        ++qord;
-        // acquire the query tile's q_scale copy (already complete: the MMA waited for it first)
-        const bool ok = timed_wait_flag(&bars[kQFull + qord % kQBufsM], (uint32_t)(qord / kQBufsM) & 1u, abort_flag, status);
-        if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      }
-      const int stage = i % kStages, a = i & 1;
+      cur.next();
+      const int slot = i % kKsSlots;
       {
-        // the accumulator, then the stage's k_scale copy and validity flag
-        bool ok = timed_wait_flag(&bars[kAFull + a], (uint32_t)(i >> 1) & 1u, abort_flag, status);
-        ok = ok && timed_wait_flag(&bars[kKFull + stage], (uint32_t)(i / kStages) & 1u, abort_flag, status);
-        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        // the item's k_scale copy and validity flag, and the accumulator
+        const uint32_t p_ks = (uint32_t)(i / kKsSlots) & 1u, p_acc = (uint32_t)(i >> 1) & 1u;
+        bool ks_ok, acc_ok;
+        mbar_test2(&bars[kKsFull + slot], p_ks, &bars[kAFull + set], p_acc, ks_ok, acc_ok);
+        if (!ks_ok) ks_ok = timed_wait_flag(&bars[kKsFull + slot], p_ks, abort_flag, status);
+        if (ks_ok && !acc_ok) acc_ok = timed_wait_flag(&bars[kAFull + set], p_acc, abort_flag, status);
+        if (!__all_sync(0xFFFFFFFFu, ks_ok && acc_ok)) break;
       }
       tc_fence_after();
-      const float ks = reinterpret_cast<const float*>(smem + kOffKs + stage * kKsBytes)[warp * 32 + lane];
-      const bool valid = valid_ring[i % kRingM] != 0;
+      const float ks = reinterpret_cast<const float*>(smem + kOffKs + slot * kKsBytes)[quarter * 32 + lane];
+      const bool valid = valid_ring[slot] != 0;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kKEmpty + stage]);  // k_scale read (the MMA commit is the other arrival)
-      const float4* qs4 = reinterpret_cast<const float4*>(smem + kOffQs + (qord % kQBufsM) * kQsBytes);
-      float acc[kTokTile] = {0.f, 0.f};
+      if (lane == 0) mbar_arrive(&bars[kKsEmpty + slot]);
+      const int t0 = shape.tok0(r) + kTokTile * tt;
+      const int nt = min(kTokTile, shape.ntok(r) - kTokTile * tt);
+      // q_scale of the tile's tokens (the same address in every lane: an L1
+      // broadcast); a one-token tile reads token 0's row twice and drops the
+      // second sum
+      const float4* qs4[kTokTile] = {reinterpret_cast<const float4*>(q_scale + (int64_t)t0 * kHeadsTc),
+                                     reinterpret_cast<const float4*>(q_scale + (int64_t)(nt > 1 ? t0 + 1 : t0) * kHeadsTc)};
+      // four partial sums per token break the FMA dependency chain
+      float part[kTokTile][4] = {};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + (uint32_t)a * kAccColsM + (uint32_t)(c * 32), v);
+        tmem_ld32(acc_addr + (uint32_t)(c * 32), v);
         tmem_wait_ld();
+        const int tok = c >> 1;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 s = qs4[(c * 32 + e) / 4];
-          float t = acc[c >> 1];
-          t = fmaf(fmaxf(__uint_as_float(v[e]), 0.f), s.x, t);
-          t = fmaf(fmaxf(__uint_as_float(v[e + 1]), 0.f), s.y, t);
-          t = fmaf(fmaxf(__uint_as_float(v[e + 2]), 0.f), s.z, t);
-          t = fmaf(fmaxf(__uint_as_float(v[e + 3]), 0.f), s.w, t);
-          acc[c >> 1] = t;
+          const float4 sc = __ldg(qs4[tok] + ((c & 1) * 32 + e) / 4);
+          part[tok][0] = fmaf(fmaxf(__uint_as_float(v[e]), 0.f), sc.x, part[tok][0]);
+          part[tok][1] = fmaf(fmaxf(__uint_as_float(v[e + 1]), 0.f), sc.y, part[tok][1]);
+          part[tok][2] = fmaf(fmaxf(__uint_as_float(v[e + 2]), 0.f), sc.z, part[tok][2]);
+          part[tok][3] = fmaf(fmaxf(__uint_as_float(v[e + 3]), 0.f), sc.w, part[tok][3]);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kAEmpty + a]);
-      const int key = kb * kPageTokens + warp * 32 + lane;
+      if (lane == 0) mbar_arrive(&bars[kAEmpty + set]);
+      const int key = kb * kPageTokens + quarter * 32 + lane;
       if (valid && key < shape.nk(r)) {
-        const int t0 = shape.tok0(r) + kTokTile * tt;
-        const int nt = min(kTokTile, shape.ntok(r) - kTokTile * tt);
-        out[(int64_t)t0 * max_keys + key] = acc[0] * ks;
-        if (nt > 1) out[(int64_t)(t0 + 1) * max_keys + key] = acc[1] * ks;
+        out[(int64_t)t0 * max_keys + key] = ((part[0][0] + part[0][1]) + (part[0][2] + part[0][3])) * ks;
+        if (nt > 1) out[(int64_t)(t0 + 1) * max_keys + key] = ((part[1][0] + part[1][1]) + (part[1][2] + part[1][3])) * ks;
       }
     }
   }
