@@ -22,27 +22,35 @@
 //                       (built on the device by the exact fp32 round-once rule,
 //                       so it is the same function; 8 copies to spread a
 //                       half-warp's reads over the banks), 9 operations per 8
-//                       elements;
-//   MMA (4 warps)       issuer e takes pages i = e (mod 4); it waits for the
+//                       elements.  Each group has one warp on each of the SM's
+//                       four sub-partitions, so the integer work is spread
+//                       evenly over them;
+//   MMA (3 warps)       issuer e takes pages i = e (mod 3); it waits for the
 //                       page's K tile (its 4 dequant warps) and for its
-//                       accumulator (the epilogue of page i - 4), then issues tcgen05.mma
-//                       kind::f8f6f4, M=128 x N=128 (keys) x K=128 (four K=32
-//                       steps) into TMEM accumulator i % 4.  MMA issue holds
-//                       its thread until the tensor core accepts the work, and
-//                       each mbarrier wait or commit costs the thread ~100-200
-//                       cycles, so one issuer's waits would idle the tensor
-//                       core; four issuers hide each other's waits;
-//   epilogue (4 warps)  warp e takes pages i = e (mod 4) and accumulator e,
+//                       accumulator (the epilogue of page i - 3), then issues
+//                       tcgen05.mma kind::f8f6f4, M=128 x N=128 (keys) x K=128
+//                       (four K=32 steps) into TMEM accumulator e.  A (the
+//                       request's query rows) is read from TMEM, so the only
+//                       shared-memory operand is the page's K tile;
+//   epilogue (3 warps)  warp e takes pages i = e (mod 3) and accumulator e,
 //                       reduces each (slot, head) row's 128 key scores with
 //                       tcgen05.ld.red (the load takes the max), applies q_scale
-//                       and stores the score.  TMEM lanes 0-31 belong to the
-//                       SM's first sub-partition, so these warps are warps 0, 4,
-//                       8 and 12 and the dequant warps live elsewhere.
+//                       and stores the score.  It also owns issuer e's query
+//                       tile in TMEM: it writes the request's 32 query rows
+//                       before the first page and rewrites them when the
+//                       request changes, after the accumulator-full wait (the
+//                       previous MMA has read them) and before releasing the
+//                       accumulator to the issuer.  TMEM lanes 0-31 belong to
+//                       the SM's first sub-partition, so these are warps 0, 4
+//                       and 8.
 //
-// The A operand is the request's 32 query rows in shared memory (2 buffers of
-// 4 KB, 128B-swizzled).  The MMA runs at M=128, so A rows 32-127 are read
-// from the 12 KB that follow the buffer; they only produce accumulator rows
-// 32-127, which nothing reads, and keep TMEM free for four accumulators.
+// Shared memory is the resource this kernel spends per page: the bulk copy
+// writes 9 KB, the dequant reads 9 KB of codes and 8 KB of table rows and
+// writes a 16 KB K tile, and the tensor core reads that tile.  Keeping the
+// query operand in TMEM spares another 16 KB per page (the MMA reads all 128
+// rows of A at M=128, though only 32 carry queries; rows 32-127 of a query
+// tile hold whatever the TMEM held and only produce accumulator rows that
+// nothing reads).
 // q_scale is applied after the max: RN multiplication is monotone, so
 // qs * max_t x_t == max_t RN(qs * x_t) for qs >= 0 (and with min for qs < 0).
 //
@@ -62,41 +70,62 @@ constexpr int kGroups = 4;      // dequant groups; group g takes pages i = g (mo
 constexpr int kGroupTiles = 2;  // K tiles per group: the group fills one while the MMA reads the other
 constexpr int kKTiles = kGroups * kGroupTiles;
 constexpr int kGroupWarps = 4;  // each warp of a group takes a quarter page (32 keys)
-constexpr int kPipe = 4;        // accumulators and epilogue warps
-constexpr int kIssuers = 4;     // MMA issuing warps; issuer e owns accumulator e
-constexpr int kQBufs = 2;       // query tiles in shared memory (request k uses k % 2)
-constexpr int kProducerWarp = 24;
-constexpr int kIssuerWarp0 = 20;
+constexpr int kPipe = 3;        // accumulators, MMA issuers and epilogue warps; issuer/epilogue e own accumulator e
+constexpr int kProducerWarp = 21;
+constexpr int kIssuerWarp0 = 17;  // warps 17, 18, 19
 constexpr int kThreads = 25 * 32;
-__host__ __device__ constexpr bool is_epi_warp(int w) { return w < 16 && (w & 3) == 0; }
-// dequant warp index 0..15 of warp w (w in 1-3, 5-7, 9-11, 13-15, 16-19)
-__device__ __forceinline__ int worker_index(int w) { return w < 16 ? w - (w >> 2) - 1 : w - 4; }
+// Warp roles by sub-partition (warp w runs on sub-partition w % 4):
+//   0: epilogue 0, 4, 8; dequant 12, 16, 20, 24
+//   1: dequant 1, 5, 9, 13; issuer 17; producer 21
+//   2: dequant 2, 6, 10, 14; issuer 18; (22 idle)
+//   3: dequant 3, 7, 11, 15; issuer 19; (23 idle)
+__host__ __device__ constexpr bool is_epi_warp(int w) { return w < 4 * kPipe && (w & 3) == 0; }
+__host__ __device__ constexpr bool is_dequant_warp(int w) {
+  return (w < 16 && (w & 3) != 0) || (w >= 12 && w <= 24 && (w & 3) == 0);
+}
+// group and in-group index (= sub-partition) of dequant warp w
+__host__ __device__ constexpr int dequant_group(int w) { return (w & 3) == 0 ? (w - 12) >> 2 : w >> 2; }
 
 constexpr int kMmaM = 128;          // query rows padded to the full datapath
 constexpr int kMmaN = kPageTokens;  // 128 keys
 constexpr uint32_t kAccCols = kMmaN;  // fp32 columns per accumulator
-constexpr uint32_t kTmemCols = 512;   // four accumulators
+constexpr uint32_t kQCols = kHeadDim / 4;  // a query tile: 128 E4M3 bytes per lane = 32 columns
+constexpr uint32_t kQCol0 = kPipe * kAccCols;  // query tile e at kQCol0 + e * kQCols
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_f8(kMmaM, kMmaN);
+static_assert(kQCol0 + kPipe * kQCols <= kTmemCols, "accumulators and query tiles fit the allocation");
 
 constexpr int kKTile = kPageTokens * kHeadDim;  // 16384
-constexpr int kQTile = kRows * kHeadDim;        // 4096: 32 rows of the A operand
+constexpr int kQBytes = kRows * kHeadDim;       // 4096: one request's 32 query rows
 constexpr int kLutCopies = 8;  // lane & 7 picks a copy
-constexpr int kRing = 32;  // page validity and page-done rings (pages in flight stay < 20 apart)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBufs * kQTile;  // A rows 32-127 of the last query buffer read K tile 0
+// Page validity ring, written by the producer, read by the dequant group and
+// the epilogue of each page.  The producer writes the slot of page i + 64
+// only after the dequant of page i + 56 has loaded its codes (raw stage
+// reuse), which waited for the MMA of page i + 48 to read its K tile (tile
+// reuse), which waited for the epilogue of page i + 45 (accumulator reuse;
+// 48 is a multiple of 3, so that is page i's epilogue warp, which works in
+// order) and for the dequant of page i + 48 (page i's group, in order).  So
+// both readers of slot i are done before it is rewritten.
+constexpr int kRing = 64;
+constexpr int kOffK = 0;
 constexpr int kOffRaw = kOffK + kKTiles * kKTile;
 constexpr int kOffLut = kOffRaw + kStages * kPageBytes;
 constexpr int kOffValid = kOffLut + 256 * 8 * kLutCopies;
-constexpr int kOffDone = kOffValid + kRing * 4;
-constexpr int kOffBar = kOffDone + kRing * 4;
-enum Bars { kRawFull = 0, kRawEmpty = kStages, kKtFull = 2 * kStages, kKtEmpty = kKtFull + kKTiles, kAccFull = kKtEmpty + kKTiles,
-            kAccEmpty = kAccFull + kPipe, kDrain = kAccEmpty + kPipe, kNumBars = kDrain + kIssuers };
+constexpr int kOffBar = kOffValid + kRing * 4;
+// K-tile full barriers are kept per (tile, issuer): pages of one tile are 8
+// apart and their issuers cycle through all three, so a single barrier per
+// tile would have three waiters, and a waiter one phase behind could pass on
+// the parity of a phase two steps on.  Barrier (t, e) serves the pages of
+// tile t issued by e, 24 apart, so each has one waiter that takes its phases
+// in order (parity (i / 24) & 1).
+constexpr int kKtPeriod = kKTiles * kPipe;  // 24
+enum Bars { kRawFull = 0, kRawEmpty = kStages, kKtFull = 2 * kStages, kKtEmpty = kKtFull + kKTiles * kPipe, kAccFull = kKtEmpty + kKTiles,
+            kAccEmpty = kAccFull + kPipe, kDrain = kAccEmpty + kPipe, kNumBars = kDrain + kPipe };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
-static_assert(kOffQ + (kQBufs - 1) * kQTile + kMmaM * kHeadDim <= kOffRaw, "A rows 32-127 stay inside the CTA's tiles");
 static_assert(kStages % kGroups == 0, "raw stage s is consumed by group s % kGroups only");
 static_assert(kStages <= 32, "one producer lane per raw stage");
-static_assert(kIssuers == kPipe, "issuer e is the only waiter of accumulator e's empty barrier");
+static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
 
 struct Misc {
   uint32_t tmem_base;
@@ -164,13 +193,20 @@ __device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, Misc*
   return false;
 }
 
-__device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity, Misc* misc, int32_t* status) {
-  if (mbar_spin(bar, parity, &misc->abort_flag)) return true;
-  if (!misc->abort_flag) {
-    misc->abort_flag = 1;
-    report(status, IDX_ST_TIMEOUT);
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+// One request's 32 query rows into a TMEM query tile: lane r of the calling
+// warp (sub-partition 0) writes row r (128 bytes, 32 columns).
+__device__ __forceinline__ void write_query_tile(uint32_t taddr, const uint8_t* q_req, int lane) {
+  uint32_t r[32];
+  const uint4* src = reinterpret_cast<const uint4*>(q_req + lane * kHeadDim);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = __ldg(src + k);
+    r[4 * k] = v.x, r[4 * k + 1] = v.y, r[4 * k + 2] = v.z, r[4 * k + 3] = v.w;
   }
-  return false;
+  tmem_st32(taddr, r);
+  tmem_wait_st();
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
@@ -186,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
   Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
   uint2* lut = reinterpret_cast<uint2*>(smem + kOffLut);
   volatile int* valid_ring = reinterpret_cast<volatile int*>(smem + kOffValid);
-  volatile int* done_ring = reinterpret_cast<volatile int*>(smem + kOffDone);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cap = min(max_blocks, width);
@@ -237,36 +272,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
   }
-  // ---- set-up: barriers, TMEM, lookup table, rings ----
+  // ---- set-up: barriers, TMEM, lookup table ----
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[kRawFull + s], 1);
       mbar_init(&bars[kRawEmpty + s], kGroupWarps);
     }
-    for (int s = 0; s < kKTiles; ++s) {
-      mbar_init(&bars[kKtFull + s], kGroupWarps);  // the tile's 4 dequant warps
-      mbar_init(&bars[kKtEmpty + s], 1);           // the MMA that read it
-    }
+    for (int s = 0; s < kKTiles * kPipe; ++s) mbar_init(&bars[kKtFull + s], kGroupWarps);  // the tile's 4 dequant warps
+    for (int s = 0; s < kKTiles; ++s) mbar_init(&bars[kKtEmpty + s], 1);                   // the MMA that read it
     for (int s = 0; s < kPipe; ++s) {
       mbar_init(&bars[kAccFull + s], 1);   // the MMA that wrote it
-      mbar_init(&bars[kAccEmpty + s], 1);  // the epilogue that read it
+      mbar_init(&bars[kAccEmpty + s], 1);  // the epilogue that read it (and wrote the query tile)
+      mbar_init(&bars[kDrain + s], 1);
     }
-    for (int s = 0; s < kIssuers; ++s) mbar_init(&bars[kDrain + s], 1);
     fence_mbar_init();
   }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&misc->tmem_base)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 0) tmem_alloc(&misc->tmem_base, kTmemCols);
   if (tid < 256) {
     // table row of scale byte s: e4m3_rn_satfinite(m * e4m3(s)) for the magnitudes m of codes 0..7
     const uint2 row = dequant8_fp32(0x76543210u, e4m3_to_f32((uint32_t)tid));
 #pragma unroll
     for (int c = 0; c < kLutCopies; ++c) lut[tid * kLutCopies + c] = row;
   }
-  if (tid < kRing) done_ring[tid] = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -314,32 +341,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     }
     // never leave with a copy in flight
     if (last >= 0) mbar_wait(&bars[kRawFull + lane], (uint32_t)(last / kStages) & 1u, nullptr);
-  } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kIssuers) {
+  } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kPipe) {
     // ---------------- MMA issuers ----------------
+    // The k-th page of issuer e waits for phase k of accumulator e's empty
+    // barrier: phase 0 is the epilogue's first query-tile write, phase k its
+    // release of page e + 3(k-1).
     const int e = warp - kIssuerWarp0;
     if (lane == 0) {
-      Cursor cur;
-      cur.init(seq_lens, num_reqs, cap, b0, j0);
-      int req_ord = cur.advance(e);
+      const uint32_t d = tmem + (uint32_t)e * kAccCols;
+      const uint32_t qa = tmem + kQCol0 + (uint32_t)e * kQCols;
       bool issued_any = false;
-      for (int i = e; i < count; i += kIssuers) {
-        const int s = i % kPipe;
+      for (int i = e; i < count; i += kPipe) {
         const int tile = (i % kGroups) * kGroupTiles + (i / kGroups) % kGroupTiles;
-        const uint32_t p_kt = (uint32_t)(i / kKTiles) & 1u, p_acc = ((uint32_t)(i / kPipe) & 1u) ^ 1u;
+        uint64_t* kt_full = &bars[kKtFull + tile * kPipe + e];
+        const uint32_t p_kt = (uint32_t)(i / kKtPeriod) & 1u, p_acc = (uint32_t)(i / kPipe) & 1u;
         bool kt_ok, acc_ok;
-        mbar_test2(&bars[kKtFull + tile], p_kt, &bars[kAccEmpty + s], p_acc, kt_ok, acc_ok);
-        if (!kt_ok && !timed_wait(&bars[kKtFull + tile], p_kt, misc, status)) break;
-        if (!acc_ok && !timed_wait(&bars[kAccEmpty + s], p_acc, misc, status)) break;
+        mbar_test2(kt_full, p_kt, &bars[kAccEmpty + e], p_acc, kt_ok, acc_ok);
+        if (!kt_ok && !timed_wait(kt_full, p_kt, misc, status)) break;
+        if (!acc_ok && !timed_wait(&bars[kAccEmpty + e], p_acc, misc, status)) break;
         tc_fence_after();
-        const uint64_t adesc = sw128_desc(sbase + kOffQ + (uint32_t)(req_ord % kQBufs) * kQTile);
         const uint64_t bdesc = sw128_desc(sbase + kOffK + (uint32_t)tile * kKTile);
-        const uint32_t d = tmem + (uint32_t)s * kAccCols;
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 32; ++kk) mma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
-        mma_commit(&bars[kAccFull + s]);
+        for (int kk = 0; kk < kHeadDim / 32; ++kk)
+          mma_f8_ta(d, qa + (uint32_t)(8 * kk), bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+        mma_commit(&bars[kAccFull + e]);
         mma_commit(&bars[kKtEmpty + tile]);
         issued_any = true;
-        req_ord += cur.advance(kIssuers);
       }
       if (issued_any) {
         // all MMAs issued by this thread complete before TMEM is freed
@@ -349,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     }
   } else if (is_epi_warp(warp)) {
     // ---------------- epilogue: lane = (slot, head) row ----------------
-    const int e = warp >> 2;  // pages i = e (mod 4), accumulator e
+    const int e = warp >> 2;  // pages i = e (mod 3), accumulator e
     Cursor cur;
     cur.init(seq_lens, num_reqs, cap, b0, j0);
     cur.advance(e);
@@ -358,9 +385,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     float qs = 0.f;
     bool neg = false;
     const uint32_t acc = tmem + (uint32_t)e * kAccCols;
+    const uint32_t qa = tmem + kQCol0 + (uint32_t)e * kQCols;
+    if (e < count) {
+      write_query_tile(qa, q + (int64_t)cur.b * kQBytes, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kAccEmpty + e]);  // phase 0: query tile ready
+    }
     for (int i = e; i < count; i += kPipe) {
       const int b = cur.b, j = cur.j;
       cur.advance(kPipe);
+      // the issuer's next page (i + 3) belongs to another request: its query
+      // rows replace this tile once page i's MMA is complete
+      const bool next_q = i + kPipe < count && cur.b != b;
+      if (next_q) prefetch_l2(q + (int64_t)cur.b * kQBytes + lane * kHeadDim);
       if (b != prev_b) {
         prev_b = b;
         qs = q_scale[(int64_t)b * kRows + lane];
@@ -370,7 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       const bool ready = timed_wait(&bars[kAccFull + e], (uint32_t)(i / kPipe) & 1u, misc, status);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;  // the TMEM loads below are warp-wide
       tc_fence_after();
-      if (lane == 0) done_ring[i % kRing] = i + 1;  // page i's MMA is complete
       const bool page_ok = valid_ring[i % kRing] != 0;
       // two reductions in flight per wait (each holds 16 registers of loaded values)
       float mx = -INFINITY, mn = INFINITY;
@@ -392,35 +429,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
           mn = fminf(mn, fminf(r0, r1));
         }
       }
+      if (next_q) write_query_tile(qa, q + (int64_t)cur.b * kQBytes, lane);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kAccEmpty + e]);  // accumulator e is free for page i + 4
+      if (lane == 0) mbar_arrive(&bars[kAccEmpty + e]);  // accumulator e (and its query tile) ready for page i + 3
       float val = qs >= 0.f ? qs * mx : qs * mn;
       if (!page_ok) val = __int_as_float(0x7FC00000);  // NaN: ranked as -inf
       if (j < own) scores[((int64_t)b * kRows + lane) * width + j] = val;
     }
-  } else if (warp < kIssuerWarp0) {
+  } else if (is_dequant_warp(warp)) {
     // ---------------- dequant: 4 groups of 4 warps ----------------
-    // group grp takes pages i = grp (mod 4) into K tile grp; warp wg of the
-    // group takes keys [32 wg, 32 wg + 32); a thread takes group pair c of keys
-    // t0 + 8k, k < 4 (16 code bytes = 32 elements, scales 2c and 2c+1 per key).
-    const int widx = worker_index(warp);
-    const int grp = widx / kGroupWarps, wg = widx % kGroupWarps;
+    // group grp takes pages i = grp (mod 4) into its K tiles; warp wg of the
+    // group (its sub-partition) takes keys [32 wg, 32 wg + 32); a thread takes
+    // group pair c of keys t0 + 8k, k < 4 (16 code bytes = 32 elements,
+    // scales 2c and 2c+1 per key).
+    const int grp = dequant_group(warp), wg = warp & 3;
     const int c = lane & 3, t0 = wg * 32 + (lane >> 2);
     const uint32_t swz0 = (uint32_t)(((2 * c) ^ (t0 & 7)) << 4), swz1 = (uint32_t)(((2 * c + 1) ^ (t0 & 7)) << 4);
     const uint2* lut_l = lut + (lane & (kLutCopies - 1));
-    Cursor cur;
-    cur.init(seq_lens, num_reqs, cap, b0, j0);
-    int req_ord = cur.advance(grp);
-    int prev_b = -1;
-    bool ok = true;
-    for (int i = grp; i < count && ok; i += kGroups) {
-      const int b = cur.b;
-      // Every group writes the query rows before its own first page of a
-      // request (identical bytes when groups overlap), so the MMA of any page
-      // depends, through that page's K-tile barrier, on a completed write.
-      const bool first_of_request = b != prev_b;
-      prev_b = b;
+    for (int i = grp; i < count; i += kGroups) {
       const int stage = i % kStages;
       const int tile = grp * kGroupTiles + (i / kGroups) % kGroupTiles;  // used by pages i, i + 8, ... of this group
       uint8_t* kd = smem + kOffK + tile * kKTile;
@@ -432,30 +459,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
         if (!raw_ok) raw_ok = timed_wait(&bars[kRawFull + stage], p_raw, misc, status);
         if (raw_ok && !kt_ok) kt_ok = timed_wait(&bars[kKtEmpty + tile], p_kt, misc, status);
         if (!__all_sync(0xFFFFFFFFu, raw_ok && kt_ok)) break;  // the warp stays converged for its ballot
-      }
-      if (first_of_request && wg == 0) {
-        // The request's 32 query rows into query buffer req_ord % 2.  Request
-        // req_ord - 2 used that buffer; its pages are < the first page of
-        // request req_ord - 1 <= i - 1, so they are <= i - 2, and every page
-        // <= i - 20 is complete (the raw ring, K tiles and accumulators bound
-        // the pages in flight), so the MMAs of pages i - 20 .. i - 2 are checked.
-        if (req_ord >= kQBufs) {
-          for (int p = max(0, i - 20) + lane; p <= i - 2; p += 32) {
-            uint32_t spins = 0;
-            while (done_ring[p % kRing] != p + 1 && ++spins < (1u << 26))
-              if ((spins & 255u) == 0 && misc->abort_flag) break;
-          }
-          __syncwarp();
-          tc_fence_after();
-        }
-        uint8_t* qt = smem + kOffQ + (req_ord % kQBufs) * kQTile;
-        const uint8_t* src = q + (int64_t)b * kQTile;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int u = lane + 32 * k, r = u >> 3, cc = u & 7;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + r * kHeadDim + cc * 16);
-          *reinterpret_cast<uint4*>(qt + r * kHeadDim + ((cc ^ (r & 7)) << 4)) = v;
-        }
       }
       // codes and scales into registers, then the raw stage goes back to the
       // producer before the (longer) dequantisation
@@ -494,15 +497,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kKtFull + tile]);
-      req_ord += cur.advance(kGroups);
+      if (lane == 0) mbar_arrive(&bars[kKtFull + tile * kPipe + i % kPipe]);  // the page's issuer is i % 3
     }
   }
 
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
