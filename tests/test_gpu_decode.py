@@ -141,6 +141,24 @@ def test_negative_and_zero_q_scale(lib):
     _check_step(wl, s, out)
 
 
+def test_signed_and_special_scales(lib):
+    """Scale bytes with the sign bit set (the product's sign flips) on every
+    other page, zero, subnormal and the largest finite scale (448) elsewhere;
+    one page holds only negative scales, so whole warps take the signed path."""
+    wl = W.decode_workload(38, 3, 3000, 9000, width=80, max_blocks=80)
+    flat = wl["kv"].reshape(wl["kv"].shape[0], -1)
+    rng = np.random.default_rng(38)
+    sc = flat[:, 8192:]
+    neg = rng.random(sc.shape) < 0.3
+    neg[1::2] = False
+    sc[neg] |= 0x80
+    special = rng.random(sc.shape) < 0.05
+    sc[special] = rng.choice(np.array([0x00, 0x01, 0x03, 0x07, 0x7E, 0x80, 0xFE], dtype=np.uint8), size=int(special.sum()))
+    sc[4] |= 0x80
+    s, out, st = _step(lib, wl)
+    _check_step(wl, s, out)
+
+
 @pytest.mark.slow
 def test_full_batched_decode_sampled(lib):
     """64 requests, seq_len U[8K, 168K], 1,344-column rows, 1% duplicated pages:
