@@ -18,12 +18,18 @@ int launch_result();
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // How rows are cut for the top-16 selector.  One warp ranks a segment of
-// 32 * per_lane columns (per_lane of 8, 16, 32, 48 or 64 values in
+// 32 * per_lane columns (per_lane of 8, 12, 16, 32, 48 or 64 values in
 // registers); a CTA of 1, 2 or 4 warps covers up to 4 segments of one row
 // (with 1 warp per row, a CTA carries 4 rows); wider rows split across
 // nsplit CTAs whose top-16s are merged through the workspace.
 constexpr int kMaxPerLane = 64;
 constexpr int kWideWarpTarget = 1216;  // 8 warps per SM: below this, halve the segments
+// Few rows of moderate width (fewer than 16 per SM of a 152-SM GPU, 257 to
+// 1,536 columns): four warps per row, 12 values per lane each, merged in
+// shared memory, so that a row's chain is a quarter as long and the GPU
+// holds four times as many warps.
+constexpr int kSplitPerLane = 12;
+constexpr int64_t kFewRows = 152 * 16;
 
 struct RowSplit {
   int per_lane;  // values per lane per segment
@@ -34,6 +40,7 @@ struct RowSplit {
 inline RowSplit row_split(int64_t rows, int32_t width) {
   const int64_t w = width <= 0 ? 1 : width;
   if (w <= 32 * kMaxPerLane) {
+    if (w > 256 && w <= 4 * 32 * kSplitPerLane && rows < kFewRows) return RowSplit{kSplitPerLane, 4, 1};
     const int need = (int)((w + 31) / 32);
     const int per_lane = need <= 8 ? 8 : need <= 16 ? 16 : need <= 32 ? 32 : need <= 48 ? 48 : 64;
     return RowSplit{per_lane, 1, 1};

@@ -406,7 +406,9 @@ int launch_rows(const PlainRows& p, const DecodeRows& d, int64_t rows, int32_t w
     else
       launch_k<kDecode, 2, 64>(p, d, rows, sp.nsplit, wsk, s);
   } else {
-    if (sp.per_lane == 32)
+    if (sp.per_lane == kSplitPerLane)
+      launch_k<kDecode, 4, kSplitPerLane>(p, d, rows, sp.nsplit, wsk, s);
+    else if (sp.per_lane == 32)
       launch_k<kDecode, 4, 32>(p, d, rows, sp.nsplit, wsk, s);
     else
       launch_k<kDecode, 4, 64>(p, d, rows, sp.nsplit, wsk, s);
