@@ -409,24 +409,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       if (!__all_sync(0xFFFFFFFFu, ready)) break;  // the TMEM loads below are warp-wide
       tc_fence_after();
       const bool page_ok = valid_ring[i % kRing] != 0;
-      // two reductions in flight per wait (each holds 16 registers of loaded values)
+      // one 32-column reduction per wait (it holds 32 registers of loaded values)
       float mx = -INFINITY, mn = INFINITY;
 #pragma unroll
       for (int c = 0; c < (int)kAccCols; c += 32) {
-        float r0, r1;
-        IDX_TMEM_LDRED16("max", acc + (uint32_t)c, r0);
-        IDX_TMEM_LDRED16("max", acc + (uint32_t)(c + 16), r1);
+        float r0;
+        IDX_TMEM_LDRED32("max", acc + (uint32_t)c, r0);
         tmem_wait_ld();
-        mx = fmaxf(mx, fmaxf(r0, r1));
+        mx = fmaxf(mx, r0);
       }
       if (neg) {
 #pragma unroll
         for (int c = 0; c < (int)kAccCols; c += 32) {
-          float r0, r1;
-          IDX_TMEM_LDRED16("min", acc + (uint32_t)c, r0);
-          IDX_TMEM_LDRED16("min", acc + (uint32_t)(c + 16), r1);
+          float r0;
+          IDX_TMEM_LDRED32("min", acc + (uint32_t)c, r0);
           tmem_wait_ld();
-          mn = fminf(mn, fminf(r0, r1));
+          mn = fminf(mn, r0);
         }
       }
       if (next_q) write_query_tile(qa, q + (int64_t)cur.b * kQBytes, lane);

@@ -109,6 +109,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     (void)r_;                                                                                           \
   } while (0)
 
+// 32 consecutive fp32 columns of this thread's TMEM lane, reduced (max or
+// min) by the load itself; the loaded values are not used.
+#define IDX_TMEM_LDRED32(OP, taddr, red)                                                                 \
+  do {                                                                                                  \
+    uint32_t r_[32];                                                                                    \
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x32." OP                                          \
+                 ".f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,"    \
+                 "%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"                                 \
+                 : "=r"(r_[0]), "=r"(r_[1]), "=r"(r_[2]), "=r"(r_[3]), "=r"(r_[4]), "=r"(r_[5]),        \
+                   "=r"(r_[6]), "=r"(r_[7]), "=r"(r_[8]), "=r"(r_[9]), "=r"(r_[10]), "=r"(r_[11]),     \
+                   "=r"(r_[12]), "=r"(r_[13]), "=r"(r_[14]), "=r"(r_[15]), "=r"(r_[16]), "=r"(r_[17]), \
+                   "=r"(r_[18]), "=r"(r_[19]), "=r"(r_[20]), "=r"(r_[21]), "=r"(r_[22]), "=r"(r_[23]), \
+                   "=r"(r_[24]), "=r"(r_[25]), "=r"(r_[26]), "=r"(r_[27]), "=r"(r_[28]), "=r"(r_[29]), \
+                   "=r"(r_[30]), "=r"(r_[31]), "=f"(red)                                                 \
+                 : "r"(taddr));                                                                         \
+    (void)r_;                                                                                           \
+  } while (0)
+
 // 2-D TMA tile load (box of the tensor map) into shared memory, completing on `bar`.
 // x is the inner coordinate (bytes for an 8-bit tensor) and must be a multiple of 16.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
