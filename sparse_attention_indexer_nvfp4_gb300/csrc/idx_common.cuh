@@ -240,6 +240,14 @@ __device__ __forceinline__ bool named_bar_red_or(int id, int threads, bool pred)
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible.  Every kernel calls it on
+// entry, before any global-memory access.  No kernel releases its
+// dependents early, so the next grid is launched as this one's CTAs exit:
+// the launch overlaps the tail instead of following the last CTA, and a
+// waiting grid never holds SM resources a running one still needs.
+__device__ __forceinline__ void pdl_enter() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Global loads / stores with cache hints
 // ---------------------------------------------------------------------------

@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(kDqThreads) k_dequant_nvfp4(const uint8_t* __r
                                                               const int32_t* __restrict__ page_offsets,
                                                               int32_t max_num_pages, uint8_t* __restrict__ out,
                                                               int64_t out_pages, int32_t* status) {
+  pdl_enter();  // before any global-memory access
   const int64_t item = blockIdx.x;
   const int r = (int)(item / max_num_pages);
   const int p = (int)(item % max_num_pages);
@@ -100,7 +101,7 @@ extern "C" int idx_dequant_nvfp4_pages(const uint8_t* kv, int64_t num_blocks, co
   if (items > 0x7FFFFFFFLL) return IDX_E_TOO_LARGE;
   int rc = check_device();
   if (rc != IDX_OK) return rc;
-  k_dequant_nvfp4<<<(unsigned)items, kDqThreads, 0, (cudaStream_t)stream>>>(
+  launch_pdl(k_dequant_nvfp4, dim3((unsigned)items), dim3(kDqThreads), 0, (cudaStream_t)stream,
       kv, num_blocks, block_table, bt_stride, max_blocks, num_pages, page_offsets, max_num_pages, out, out_pages,
       status);
   return launch_result();

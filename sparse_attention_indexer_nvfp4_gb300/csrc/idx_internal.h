@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "idx.h"
 
@@ -16,6 +17,27 @@ int check_device();
 int launch_result();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Launch with programmatic dependent launch allowed: the grid may be launched
+// while the previous kernel in the stream is still finishing, so its launch
+// and CTA scheduling overlap that kernel's tail.  Every kernel of this
+// library waits for the grids it depends on (griddepcontrol.wait) before it
+// touches global memory, so results are those of ordinary stream order.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // How rows are cut for the top-16 selector.  One warp ranks a segment of
 // 32 * per_lane columns (per_lane of 8, 12, 16, 32, 48 or 64 values in

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kMtpThreads) k_mtp_fma(const uint8_t* __restri
                                                          int32_t max_blocks, const int32_t* __restrict__ num_keys,
                                                          const int32_t* __restrict__ cu_tokens, int32_t num_tokens,
                                                          int32_t max_keys, float* __restrict__ out, int32_t* status) {
+  pdl_enter();  // before any global-memory access
   extern __shared__ float smem[];
   float* kf = smem;                              // [128][129]
   float* qf = kf + kPageTokens * kKPad;          // [heads][128]
@@ -71,7 +72,7 @@ int launch_mtp_fma(const uint8_t* q, const float* q_scale, int32_t num_tokens, i
     return IDX_E_CUDA;
   const int tiles = (min(max_keys, max_blocks * kPageTokens) + kPageTokens - 1) / kPageTokens;
   if (tiles <= 0) return IDX_OK;
-  k_mtp_fma<<<dim3((unsigned)tiles, (unsigned)num_reqs), kMtpThreads, kMtpSmem, stream>>>(
+  launch_pdl(k_mtp_fma, dim3((unsigned)tiles, (unsigned)num_reqs), dim3(kMtpThreads), kMtpSmem, stream,
       q, q_scale, heads, k, k_scale, num_blocks, bt, bt_stride, max_blocks, num_keys, cu_tokens, num_tokens, max_keys, out,
       status);
   return launch_result();

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
                                                       const int32_t* __restrict__ bt, int64_t bt_stride,
                                                       ReqShape shape, int32_t max_keys, float* __restrict__ out,
                                                       int32_t* status) {
+  pdl_enter();  // before any global-memory access
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -342,6 +343,13 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
         uint32_t v[32];
         tmem_ld32(acc_addr + (uint32_t)(c * 32), v);
         tmem_wait_ld();
+        if (c == 3) {
+          // every column is in registers: the accumulator goes back to the MMA
+          // before the last chunk's arithmetic
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kAEmpty + set]);
+        }
         const int tok = c >> 1;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -352,9 +360,6 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
           part[tok][3] = fmaf(fmaxf(__uint_as_float(v[e + 3]), 0.f), sc.w, part[tok][3]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kAEmpty + set]);
       const int key = kb * kPageTokens + quarter * 32 + lane;
       if (valid && key < shape.nk(r)) {
         out[(int64_t)t0 * max_keys + key] = ((part[0][0] + part[0][1]) + (part[0][2] + part[0][3])) * ks;
@@ -430,7 +435,7 @@ int launch_mtp_tc(const uint8_t* q, const float* q_scale, int32_t num_tokens, co
   ReqShape sh{num_keys, cu_tokens, num_reqs, num_tokens, (int)std::min<int64_t>(max_keys, (int64_t)max_blocks * 128)};
   // two CTAs per SM: 256 TMEM columns and ~100 KB of shared memory each
   const int grid = 2 * g_sms_m[dev];
-  k_mtp_tc<<<grid, kThreadsM, kSmemM, stream>>>(kmap, qmap, q_scale, k_scale, num_blocks, bt, bt_stride, sh, max_keys,
+  launch_pdl(k_mtp_tc, dim3(grid), dim3(kThreadsM), kSmemM, stream, kmap, qmap, q_scale, k_scale, num_blocks, bt, bt_stride, sh, max_keys,
                                                  out, status);
   return launch_result();
 }

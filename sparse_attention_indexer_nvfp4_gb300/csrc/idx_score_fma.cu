@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kFmaThreads) k_score_fma(const uint8_t* __rest
                                                            int32_t max_blocks, const int32_t* __restrict__ seq_lens,
                                                            int32_t query_len, int32_t width, float* __restrict__ scores,
                                                            int32_t* status) {
+  pdl_enter();  // before any global-memory access
   extern __shared__ float smem[];
   float* qf = smem;                       // [32][128]
   float* kf = smem + kRows * kHeadDim;    // [128][129]
@@ -121,7 +122,7 @@ int launch_score_fma(const uint8_t* q, const float* q_scale, const uint8_t* kv, 
   const int cols = min(width, max_blocks);
   if (cols <= 0) return IDX_OK;
   const dim3 grid((unsigned)cols, (unsigned)num_reqs);
-  k_score_fma<<<grid, kFmaThreads, kFmaSmem, stream>>>(q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks, seq_lens,
+  launch_pdl(k_score_fma, grid, dim3(kFmaThreads), kFmaSmem, stream, q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks, seq_lens,
                                                        query_len, width, scores, status);
   return launch_result();
 }

@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     int64_t num_blocks, const int32_t* __restrict__ bt, int64_t bt_stride, int32_t max_blocks,
     const int32_t* __restrict__ seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
     float* __restrict__ scores, int32_t* status) {
+  pdl_enter();  // before any global-memory access
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -528,7 +529,7 @@ int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, i
   if (upper <= 0) return IDX_OK;
   // one CTA per SM: each CTA holds all 512 TMEM columns of its SM
   const int grid = (int)std::min<int64_t>((int64_t)g_sms[dev], upper);
-  k_score_decode<<<grid, kThreads, kSmemBytes, stream>>>(q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks,
+  launch_pdl(k_score_decode, dim3(grid), dim3(kThreads), kSmemBytes, stream, q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks,
                                                           seq_lens, num_reqs, query_len, width, scores, status);
   return launch_result();
 }

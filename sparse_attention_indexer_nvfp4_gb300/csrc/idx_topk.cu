@@ -307,6 +307,7 @@ __device__ __forceinline__ void decode_write(const DecodeRows& d, int64_t r, int
 // ws[(row * nsplit + split) * 16].
 template <int kWarps, bool kDecode, int K>
 __global__ void __launch_bounds__(128) k_topk_rows(PlainRows p, DecodeRows d, int64_t rows, int nsplit, uint64_t* ws) {
+  pdl_enter();  // before any global-memory access
   constexpr int kCtaWarps = kWarps == 1 ? 4 : kWarps;
   constexpr int kSeg = 32 * K;
   __shared__ WarpScratch scratch[kCtaWarps];
@@ -352,6 +353,7 @@ __global__ void __launch_bounds__(128) k_topk_rows(PlainRows p, DecodeRows d, in
 template <bool kDecode>
 __global__ void __launch_bounds__(128) k_topk_merge(PlainRows p, DecodeRows d, int64_t rows, int nsplit,
                                                     const uint64_t* __restrict__ ws) {
+  pdl_enter();  // before any global-memory access
   __shared__ WarpScratch scratch[4];
   const int64_t r = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (r >= rows) return;
@@ -382,7 +384,7 @@ __global__ void __launch_bounds__(128) k_topk_merge(PlainRows p, DecodeRows d, i
 template <bool kDecode, int kWarps, int K>
 void launch_k(const PlainRows& p, const DecodeRows& d, int64_t rows, int nsplit, uint64_t* ws, cudaStream_t s) {
   const dim3 grid(kWarps == 1 ? (unsigned)((rows + 3) / 4) : (unsigned)rows, (unsigned)nsplit);
-  k_topk_rows<kWarps, kDecode, K><<<grid, (kWarps == 1 ? 4 : kWarps) * 32, 0, s>>>(p, d, rows, nsplit, ws);
+  launch_pdl(k_topk_rows<kWarps, kDecode, K>, grid, dim3((kWarps == 1 ? 4 : kWarps) * 32), 0, s, p, d, rows, nsplit, ws);
 }
 
 template <bool kDecode>
@@ -415,7 +417,8 @@ int launch_rows(const PlainRows& p, const DecodeRows& d, int64_t rows, int32_t w
   }
   int rc = launch_result();
   if (rc != IDX_OK || sp.nsplit == 1) return rc;
-  k_topk_merge<kDecode><<<(unsigned)((rows + 3) / 4), 128, 0, s>>>(p, d, rows, sp.nsplit, wsk);
+  launch_pdl(k_topk_merge<kDecode>, dim3((unsigned)((rows + 3) / 4)), dim3(128), 0, s, p, d, rows, sp.nsplit,
+             (const uint64_t*)wsk);
   return launch_result();
 }
 
