@@ -222,22 +222,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // proxy (the tensor cores read operands through it).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// bar.red.or on named barrier `id` over `threads` threads: waits for all of
-// them and returns whether any passed true (with bar.sync's memory ordering).
-__device__ __forceinline__ bool named_bar_red_or(int id, int threads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %3, 0;\n\tbar.red.or.pred q, %1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(id), "r"(threads), "r"((uint32_t)pred)
-      : "memory");
-  return r != 0;
-}
-
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 // Programmatic dependent launch: wait until the grids this one depends on

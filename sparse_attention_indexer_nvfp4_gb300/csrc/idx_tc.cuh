@@ -39,16 +39,6 @@ __device__ __forceinline__ void mma_f8_ta(uint32_t d_tmem, uint32_t a_tmem, uint
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
-// Weight-stationary form, D[tmem] (+)= A[smem] * B[smem]^T.  At M=32, N=128
-// the 32 x 128 fp32 result occupies 32 TMEM columns of all 128 lanes: row r,
-// column n sits in lane 32 * (n / 32) + r, column n % 32.
-__device__ __forceinline__ void mma_f8_ws(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.ws.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
