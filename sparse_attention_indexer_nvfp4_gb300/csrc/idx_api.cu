@@ -1,6 +1,9 @@
 // Host entry points of the C ABI that are not tied to one kernel file:
 // error text, device check, the decode scorer dispatch and the decode step.
+#include <cudaTypedefs.h>
+
 #include <cstdio>
+#include <mutex>
 
 #include "idx_common.cuh"
 #include "idx_internal.h"
@@ -31,6 +34,28 @@ int check_device() {
     g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
   }
   return g_device_ok[dev] == 1 ? IDX_OK : IDX_E_DEVICE;
+}
+
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, const void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (encode == nullptr) {
+      cudaDriverEntryPointQueryResult qr;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+              cudaSuccess ||
+          qr != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  return encode(map, type, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int launch_result() {

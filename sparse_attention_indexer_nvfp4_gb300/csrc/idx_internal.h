@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <utility>
 
@@ -17,6 +18,13 @@ int check_device();
 int launch_result();
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point
+// (looked up once per process).  Returns false when the entry point is
+// missing or the driver rejects the description.
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, const void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       CUtensorMapSwizzle swizzle);
 
 // Launch with programmatic dependent launch allowed: the grid may be launched
 // while the previous kernel in the stream is still finishing, so its launch

@@ -25,10 +25,6 @@
 // The key tiles go back to the producer as soon as the MMA has read them;
 // k_scale and the validity flag travel in a separate, deeper ring that the
 // epilogue releases.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "idx_common.cuh"
 #include "idx_internal.h"
 #include "idx_tc.cuh"
@@ -375,8 +371,6 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::mutex g_encode_mu;
 int g_sms_m[64];
 bool g_attr_m[64];
 
@@ -384,10 +378,7 @@ bool encode_2d_u8(CUtensorMap* map, const void* base, uint64_t rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
   const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, 128u};
-  const cuuint32_t estr[2] = {1u, 1u};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tensor_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
@@ -408,25 +399,13 @@ int launch_mtp_tc(const uint8_t* q, const float* q_scale, int32_t num_tokens, co
                   cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IDX_E_CUDA;
-  {
-    std::lock_guard<std::mutex> lock(g_encode_mu);
-    if (g_encode == nullptr) {
-      cudaDriverEntryPointQueryResult qr;
-      void* fn = nullptr;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
-              cudaSuccess ||
-          qr != cudaDriverEntryPointSuccess || fn == nullptr)
-        return IDX_E_CUDA;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    if (!g_attr_m[dev]) {
-      if (cudaFuncSetAttribute(k_mtp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemM) != cudaSuccess ||
-          cudaFuncSetAttribute(k_mtp_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-          cudaDeviceGetAttribute(&g_sms_m[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return IDX_E_CUDA;
-      g_attr_m[dev] = true;
-    }
+  if (!g_attr_m[dev]) {
+    if (cudaFuncSetAttribute(k_mtp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemM) != cudaSuccess ||
+        cudaFuncSetAttribute(k_mtp_tc, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+        cudaDeviceGetAttribute(&g_sms_m[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return IDX_E_CUDA;
+    g_attr_m[dev] = true;
   }
   CUtensorMap kmap, qmap;
   if (!encode_2d_u8(&kmap, k, (uint64_t)num_blocks * kPageTokens) ||

@@ -12,8 +12,8 @@
 //
 //   producer (1 warp)   raw NVFP4 page -> 8-stage shared-memory ring, one
 //                       9,216-byte bulk copy per page (a 72-byte row is not a
-//                       legal TMA box); lane s refills stage s, so the eight
-//                       stages are refilled in parallel;
+//                       legal TMA box); lane s refills stage s as soon as
+//                       it is free, polling its own empty barrier;
 //   dequant (16 warps)  4 groups of 4 warps, group g takes pages i = g (mod 4)
 //                       and owns two K tiles (one filled while the MMA reads
 //                       the other): the page becomes a 128B-swizzled
@@ -25,7 +25,8 @@
 //                       elements.  Each group has one warp on each of the SM's
 //                       four sub-partitions, so the integer work is spread
 //                       evenly over them;
-//   MMA (3 warps)       issuer e takes pages i = e (mod 3); it waits for the
+//   MMA (3 warps)       issuer e takes pages i = e (mod 3) (one elected
+//                       thread of the converged warp issues); it waits for the
 //                       page's K tile (its 4 dequant warps) and for its
 //                       accumulator (the epilogue of page i - 3), then issues
 //                       tcgen05.mma kind::f8f6f4, M=128 x N=128 (keys) x K=128
@@ -74,6 +75,7 @@ constexpr int kPipe = 3;        // accumulators, MMA issuers and epilogue warps;
 constexpr int kProducerWarp = 21;
 constexpr int kIssuerWarp0 = 17;  // warps 17, 18, 19
 constexpr int kThreads = 25 * 32;
+constexpr uint32_t kProducerIdleLimit = 1u << 24;  // idle polls (~64 ns back-off each) before a timeout
 // Warp roles by sub-partition (warp w runs on sub-partition w % 4):
 //   0: epilogue 0, 4, 8; dequant 12, 16, 20, 24
 //   1: dequant 1, 5, 9, 13; issuer 17; producer 21
@@ -304,41 +306,62 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
   if (warp == kProducerWarp) {
     // ---------------- producer: raw pages into the ring ----------------
     // Lane s < kStages owns ring stage s and fills it with pages i = s (mod
-    // kStages): the stages are refilled in parallel, one wait and one bulk
-    // copy per lane per round, instead of one serial wait + copy chain per
-    // page (each mbarrier operation costs the issuing thread ~100+ cycles).
-    // Block ids are loaded one round ahead.
+    // kStages).  Each lane polls its own stage's empty barrier without
+    // blocking, so a stage is refilled as soon as its dequant group has
+    // loaded the page it held, whatever the other stages are doing: with a
+    // blocking wait per lane the warp moved on only when the slowest stage
+    // of a round of eight was free, and early stages stood empty for most of
+    // a round.  Block ids are loaded one page ahead.
     const bool owner = lane < kStages;
     Cursor lc;
     lc.init(seq_lens, num_reqs, cap, b0, j0);
     if (owner) lc.advance(lane);
-    int64_t blk = (owner && lane < count) ? (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j] : -1;
-    int last = -1;  // the last page this lane issued into its stage
-    for (int base = 0; base < count; base += kStages) {
-      const int i = base + lane;
+    int i = lane;  // the next page this lane copies
+    int64_t blk = (owner && i < count) ? (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j] : -1;
+    int64_t blk_next = -1;
+    if (owner && i + kStages < count) {
+      lc.advance(kStages);
+      blk_next = (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j];
+    }
+    int last = -1;      // the last page this lane copied into its stage
+    uint32_t idle = 0;  // polls in a row without progress in any lane
+    while (true) {
       const bool active = owner && i < count;
-      int64_t blk_next = -1;
-      if (active && i + kStages < count) {
-        lc.advance(kStages);
-        blk_next = (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j];
-      }
-      bool ok = true;
-      if (active) {
-        ok = timed_wait(&bars[kRawEmpty + lane], ((uint32_t)(i / kStages) & 1u) ^ 1u, misc, status);
-        if (ok) {
-          const bool valid = blk >= 0 && blk < num_blocks;
-          valid_ring[i % kRing] = valid ? 1 : 0;
-          if (valid) {
-            mbar_arrive_expect_tx(&bars[kRawFull + lane], kPageBytes);
-            bulk_g2s(smem + kOffRaw + lane * kPageBytes, kv + blk * kPageBytes, kPageBytes, &bars[kRawFull + lane]);
-          } else {
-            mbar_arrive(&bars[kRawFull + lane]);
-          }
-          last = i;
+      if (!__any_sync(0xFFFFFFFFu, active)) break;
+      bool progressed = false;
+      if (active && mbar_try_wait_nosuspend(&bars[kRawEmpty + lane], ((uint32_t)(i / kStages) & 1u) ^ 1u)) {
+        const bool valid = blk >= 0 && blk < num_blocks;
+        valid_ring[i % kRing] = valid ? 1 : 0;
+        if (valid) {
+          mbar_arrive_expect_tx(&bars[kRawFull + lane], kPageBytes);
+          bulk_g2s(smem + kOffRaw + lane * kPageBytes, kv + blk * kPageBytes, kPageBytes, &bars[kRawFull + lane]);
+        } else {
+          mbar_arrive(&bars[kRawFull + lane]);
         }
+        last = i;
+        i += kStages;
+        blk = blk_next;
+        blk_next = -1;
+        if (i + kStages < count) {
+          lc.advance(kStages);
+          blk_next = (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j];
+        }
+        progressed = true;
       }
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      blk = blk_next;
+      if (__any_sync(0xFFFFFFFFu, progressed)) {
+        idle = 0;
+        continue;
+      }
+      // Nothing freed: back off briefly; give up (a few seconds) like the
+      // bounded waits, or when another role has given up.
+      if (++idle > kProducerIdleLimit || *reinterpret_cast<volatile int*>(&misc->abort_flag)) {
+        if (lane == 0 && !misc->abort_flag) {
+          misc->abort_flag = 1;
+          report(status, IDX_ST_TIMEOUT);
+        }
+        break;
+      }
+      __nanosleep(64);
     }
     // never leave with a copy in flight
     if (last >= 0) mbar_wait(&bars[kRawFull + lane], (uint32_t)(last / kStages) & 1u, nullptr);
@@ -347,33 +370,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     // The k-th page of issuer e waits for phase k of accumulator e's empty
     // barrier: phase 0 is the epilogue's first query-tile write, phase k its
     // release of page e + 3(k-1).
+    // The loop runs on the whole (converged) warp, so every operand of the
+    // MMAs is warp-uniform, and one elected thread issues them: from a
+    // single-thread branch a page's four MMAs took about twice as long to
+    // issue.
     const int e = warp - kIssuerWarp0;
-    if (lane == 0) {
-      const uint32_t d = tmem + (uint32_t)e * kAccCols;
-      const uint32_t qa = tmem + kQCol0 + (uint32_t)e * kQCols;
-      bool issued_any = false;
-      for (int i = e; i < count; i += kPipe) {
-        const int tile = (i % kGroups) * kGroupTiles + (i / kGroups) % kGroupTiles;
-        uint64_t* kt_full = &bars[kKtFull + tile * kPipe + e];
-        const uint32_t p_kt = (uint32_t)(i / kKtPeriod) & 1u, p_acc = (uint32_t)(i / kPipe) & 1u;
-        bool kt_ok, acc_ok;
-        mbar_test2(kt_full, p_kt, &bars[kAccEmpty + e], p_acc, kt_ok, acc_ok);
-        if (!kt_ok && !timed_wait(kt_full, p_kt, misc, status)) break;
-        if (!acc_ok && !timed_wait(&bars[kAccEmpty + e], p_acc, misc, status)) break;
-        tc_fence_after();
+    const uint32_t d = tmem + (uint32_t)e * kAccCols;
+    const uint32_t qa = tmem + kQCol0 + (uint32_t)e * kQCols;
+    bool issued_any = false;
+    for (int i = e; i < count; i += kPipe) {
+      const int tile = (i % kGroups) * kGroupTiles + (i / kGroups) % kGroupTiles;
+      uint64_t* kt_full = &bars[kKtFull + tile * kPipe + e];
+      const uint32_t p_kt = (uint32_t)(i / kKtPeriod) & 1u, p_acc = (uint32_t)(i / kPipe) & 1u;
+      bool kt_ok, acc_ok;
+      mbar_test2(kt_full, p_kt, &bars[kAccEmpty + e], p_acc, kt_ok, acc_ok);
+      if (!kt_ok) kt_ok = timed_wait(kt_full, p_kt, misc, status);
+      if (kt_ok && !acc_ok) acc_ok = timed_wait(&bars[kAccEmpty + e], p_acc, misc, status);
+      if (!__all_sync(0xFFFFFFFFu, kt_ok && acc_ok)) break;
+      tc_fence_after();
+      if (elect_one()) {
         const uint64_t bdesc = sw128_desc(sbase + kOffK + (uint32_t)tile * kKTile);
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 32; ++kk)
           mma_f8_ta(d, qa + (uint32_t)(8 * kk), bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
         mma_commit(&bars[kAccFull + e]);
         mma_commit(&bars[kKtEmpty + tile]);
-        issued_any = true;
       }
-      if (issued_any) {
-        // all MMAs issued by this thread complete before TMEM is freed
-        mma_commit(&bars[kDrain + e]);
-        mbar_wait(&bars[kDrain + e], 0, nullptr);
-      }
+      __syncwarp();
+      issued_any = true;
+    }
+    if (issued_any) {
+      // all MMAs issued by this warp complete before TMEM is freed
+      if (elect_one()) mma_commit(&bars[kDrain + e]);
+      __syncwarp();
+      mbar_wait(&bars[kDrain + e], 0, nullptr);
     }
   } else if (is_epi_warp(warp)) {
     // ---------------- epilogue: lane = (slot, head) row ----------------

@@ -127,6 +127,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// One thread of the (converged) warp is elected: true in that thread only.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b32 R;\n\telect.sync R|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Bounded waits that record a timeout in `status` and raise the CTA's abort flag.
 __device__ __forceinline__ bool timed_wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                 int32_t* status) {
