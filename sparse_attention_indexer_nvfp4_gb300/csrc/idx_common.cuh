@@ -27,6 +27,16 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status != nullptr) atomicOr(status, bits);
 }
 
+// Sum of v over the 32 lanes of the (converged) warp, in every lane.  A
+// CTA-wide total is formed from one shared-memory atomic per warp: a 64-bit
+// shared-memory atomic from every thread serialised into microseconds of
+// retries at kernel start.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
 // floor((a) / 128) for possibly negative a
 __device__ __forceinline__ int floor_div_page(int a) { return a >= 0 ? a / kPageTokens : -((-a + kPageTokens - 1) / kPageTokens); }
 

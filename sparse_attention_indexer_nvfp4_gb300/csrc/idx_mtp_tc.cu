@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
   {
     unsigned long long local = 0;
     for (int r = tid; r < shape.R; r += kThreadsM) local += (unsigned long long)shape.items(r);
-    if (local) atomicAdd(&misc->total, local);
+    local = warp_sum_u64(local);
+    if ((tid & 31) == 0 && local) atomicAdd(&misc->total, local);
   }
   __syncthreads();
   const unsigned long long W = misc->total;

@@ -244,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       clamped |= floor_div_page(seq - 1) > cap;
     }
     if (clamped && blockIdx.x == 0) report(status, IDX_ST_LEN_CLAMPED);
-    if (local) atomicAdd(&misc->total, local);
+    local = warp_sum_u64(local);
+    if ((tid & 31) == 0 && local) atomicAdd(&misc->total, local);
   }
   __syncthreads();
   const unsigned long long P = misc->total;
