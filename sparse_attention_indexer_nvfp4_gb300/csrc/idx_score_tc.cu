@@ -442,22 +442,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       tc_fence_after();
       const bool page_ok = valid_ring[i % kRing] != 0;
       // one 32-column reduction per wait (it holds 32 registers of loaded values)
-      float mx = -INFINITY, mn = INFINITY;
-#pragma unroll
-      for (int c = 0; c < (int)kAccCols; c += 32) {
-        float r0;
-        IDX_TMEM_LDRED32("max", acc + (uint32_t)c, r0);
+      // three rounds of loads in flight (32 + 16, 32 + 16, 32 columns): the
+      // register budget holds 48 loaded values at a time
+      float mx, mn = INFINITY;
+      {
+        float r0, r1, r2, r3, r4;
+        IDX_TMEM_LDRED32("max", acc, r0);
+        IDX_TMEM_LDRED16("max", acc + 32u, r1);
         tmem_wait_ld();
-        mx = fmaxf(mx, r0);
+        IDX_TMEM_LDRED32("max", acc + 48u, r2);
+        IDX_TMEM_LDRED16("max", acc + 80u, r3);
+        tmem_wait_ld();
+        IDX_TMEM_LDRED32("max", acc + 96u, r4);
+        tmem_wait_ld();
+        mx = fmaxf(fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)), r4);
       }
       if (neg) {
-#pragma unroll
-        for (int c = 0; c < (int)kAccCols; c += 32) {
-          float r0;
-          IDX_TMEM_LDRED32("min", acc + (uint32_t)c, r0);
-          tmem_wait_ld();
-          mn = fminf(mn, r0);
-        }
+        float r0, r1, r2, r3, r4;
+        IDX_TMEM_LDRED32("min", acc, r0);
+        IDX_TMEM_LDRED16("min", acc + 32u, r1);
+        tmem_wait_ld();
+        IDX_TMEM_LDRED32("min", acc + 48u, r2);
+        IDX_TMEM_LDRED16("min", acc + 80u, r3);
+        tmem_wait_ld();
+        IDX_TMEM_LDRED32("min", acc + 96u, r4);
+        tmem_wait_ld();
+        mn = fminf(fminf(fminf(r0, r1), fminf(r2, r3)), r4);
       }
       if (next_q) write_query_tile(qa, q + (int64_t)cur.b * kQBytes, lane);
       tc_fence_before();
