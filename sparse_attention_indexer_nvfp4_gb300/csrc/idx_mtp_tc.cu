@@ -56,7 +56,9 @@ enum BarsM { kKFull = 0, kKEmpty = kStages, kQFull = 2 * kStages, kQEmpty = kQFu
              kAFull = kQEmpty + kQBufsM, kAEmpty = kAFull + 2, kKsFull = kAEmpty + 2, kKsEmpty = kKsFull + kKsSlots,
              kDrainM = kKsEmpty + kKsSlots, kNumBarsM };
 constexpr int kOffMiscM = kOffBarM + kNumBarsM * 8;
-constexpr int kSmemM = kOffMiscM + 64 + 1024;
+constexpr int kOffReqItems = kOffMiscM + 64;  // [kThreadsM] int: items of the first kThreadsM requests
+constexpr int kSmemM = kOffReqItems + kThreadsM * 4 + 1024;
+static_assert(2 * (kSmemM + 1024) <= 233472, "two CTAs (and their reserved shared memory) fit one SM");
 
 struct MiscM {
   uint32_t tmem_base;
@@ -129,7 +131,12 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
   __syncthreads();
   {
     unsigned long long local = 0;
-    for (int r = tid; r < shape.R; r += kThreadsM) local += (unsigned long long)shape.items(r);
+    int* req_items = reinterpret_cast<int*>(smem + kOffReqItems);
+    for (int r = tid; r < shape.R; r += kThreadsM) {
+      const int n = shape.items(r);
+      if (r < kThreadsM) req_items[r] = n;  // the slice search below reads these from shared memory
+      local += (unsigned long long)n;
+    }
     local = warp_sum_u64(local);
     if ((tid & 31) == 0 && local) atomicAdd(&misc->total, local);
   }
@@ -142,7 +149,9 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
     unsigned long long acc = 0;
     for (int base = 0; base < shape.R; base += 32) {
       const int r = base + lane;
-      const unsigned long long n = r < shape.R ? (unsigned long long)shape.items(r) : 0ull;
+      const int* req_items = reinterpret_cast<const int*>(smem + kOffReqItems);
+      const unsigned long long n =
+          r >= shape.R ? 0ull : (unsigned long long)(r < kThreadsM ? req_items[r] : shape.items(r));
       unsigned long long incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {

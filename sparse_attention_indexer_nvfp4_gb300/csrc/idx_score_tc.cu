@@ -124,7 +124,8 @@ constexpr int kKtPeriod = kKTiles * kPipe;  // 24
 enum Bars { kRawFull = 0, kRawEmpty = kStages, kKtFull = 2 * kStages, kKtEmpty = kKtFull + kKTiles * kPipe, kAccFull = kKtEmpty + kKTiles,
             kAccEmpty = kAccFull + kPipe, kDrain = kAccEmpty + kPipe, kNumBars = kDrain + kPipe };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
+constexpr int kOffReqPages = kOffMisc + 64;  // [kThreads] int: pages of the first kThreads requests
+constexpr int kSmemBytes = kOffReqPages + kThreads * 4 + 1024;  // + slack to align the base to 1024
 static_assert(kStages % kGroups == 0, "raw stage s is consumed by group s % kGroups only");
 static_assert(kStages <= 32, "one producer lane per raw stage");
 static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
@@ -238,9 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
   {
     unsigned long long local = 0;
     bool clamped = false;
+    int* req_pages = reinterpret_cast<int*>(smem + kOffReqPages);
     for (int b = tid; b < num_reqs; b += kThreads) {
       const int seq = seq_lens[b];
-      local += (unsigned long long)pages_of(seq, cap);
+      const int n = pages_of(seq, cap);
+      if (b < kThreads) req_pages[b] = n;  // the slice search below reads these from shared memory
+      local += (unsigned long long)n;
       clamped |= floor_div_page(seq - 1) > cap;
     }
     if (clamped && blockIdx.x == 0) report(status, IDX_ST_LEN_CLAMPED);
@@ -256,7 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     unsigned long long acc = 0;
     for (int base = 0; base < num_reqs; base += 32) {
       const int b = base + lane;
-      const unsigned long long n = b < num_reqs ? (unsigned long long)pages_of(seq_lens[b], cap) : 0ull;
+      const int* req_pages = reinterpret_cast<const int*>(smem + kOffReqPages);
+      const unsigned long long n =
+          b >= num_reqs ? 0ull : (unsigned long long)(b < kThreads ? req_pages[b] : pages_of(seq_lens[b], cap));
       unsigned long long incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
