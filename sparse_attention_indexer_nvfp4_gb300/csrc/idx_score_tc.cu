@@ -41,9 +41,11 @@
 //                       before the first page and rewrites them when the
 //                       request changes, after the accumulator-full wait (the
 //                       previous MMA has read them) and before releasing the
-//                       accumulator to the issuer.  TMEM lanes 0-31 belong to
-//                       the SM's first sub-partition, so these are warps 0, 4
-//                       and 8.
+//                       accumulator to the issuer.  The query rows (and so the
+//                       accumulator's rows of scores) sit in the TMEM lane
+//                       quarter of the epilogue warp's sub-partition: lanes
+//                       0-31 for accumulators 0 and 1 (warps 0 and 4), lanes
+//                       32-63 for accumulator 2 (warp 1).
 //
 // Shared memory is the resource this kernel spends per page: the bulk copy
 // writes 9 KB, the dequant reads 9 KB of codes and 8 KB of table rows and
@@ -72,21 +74,27 @@ constexpr int kGroupTiles = 2;  // K tiles per group: the group fills one while 
 constexpr int kKTiles = kGroups * kGroupTiles;
 constexpr int kGroupWarps = 4;  // each warp of a group takes a quarter page (32 keys)
 constexpr int kPipe = 3;        // accumulators, MMA issuers and epilogue warps; issuer/epilogue e own accumulator e
-constexpr int kProducerWarp = 21;
-constexpr int kIssuerWarp0 = 17;  // warps 17, 18, 19
-constexpr int kThreads = 25 * 32;
+constexpr int kProducerWarp = 2;
+constexpr int kThreads = 23 * 32;
 constexpr uint32_t kProducerIdleLimit = 1u << 24;  // idle polls (~64 ns back-off each) before a timeout
-// Warp roles by sub-partition (warp w runs on sub-partition w % 4):
-//   0: epilogue 0, 4, 8; dequant 12, 16, 20, 24
-//   1: dequant 1, 5, 9, 13; issuer 17; producer 21
-//   2: dequant 2, 6, 10, 14; issuer 18; (22 idle)
-//   3: dequant 3, 7, 11, 15; issuer 19; (23 idle)
-__host__ __device__ constexpr bool is_epi_warp(int w) { return w < 4 * kPipe && (w & 3) == 0; }
-__host__ __device__ constexpr bool is_dequant_warp(int w) {
-  return (w < 16 && (w & 3) != 0) || (w >= 12 && w <= 24 && (w & 3) == 0);
-}
-// group and in-group index (= sub-partition) of dequant warp w
-__host__ __device__ constexpr int dequant_group(int w) { return (w & 3) == 0 ? (w - 12) >> 2 : w >> 2; }
+// Warp roles by sub-partition (warp w runs on sub-partition w % 4; at most
+// six warps on one, so 80 registers per thread -- with seven on one the cap
+// was 72 and the epilogue's page bookkeeping spilled to local memory, inside
+// the accumulator's round trip):
+//   0: epilogue 0 (warp 0), epilogue 1 (4); dequant 8, 12, 16, 20
+//   1: epilogue 2 (1); issuer 0 (5); dequant 9, 13, 17, 21
+//   2: producer (2); issuer 1 (6); dequant 10, 14, 18, 22
+//   3: issuer 2 (3); dequant 7, 11, 15, 19
+// Accumulator e's query rows, and so its rows of scores, sit in TMEM lane
+// quarter epi_quarter(e): the sub-partition of its epilogue warp.
+__host__ __device__ constexpr int epi_of(int w) { return w == 0 ? 0 : w == 4 ? 1 : w == 1 ? 2 : -1; }
+__host__ __device__ constexpr int epi_quarter(int e) { return e == 2 ? 1 : 0; }
+__host__ __device__ constexpr int issuer_of(int w) { return w == 5 ? 0 : w == 6 ? 1 : w == 3 ? 2 : -1; }
+__host__ __device__ constexpr bool is_dequant_warp(int w) { return w >= 7 && w < 23; }
+// group of dequant warp w (its in-group index is its sub-partition w % 4)
+__host__ __device__ constexpr int dequant_group(int w) { return (w - 7) >> 2; }
+static_assert(epi_quarter(0) == (0 & 3) && epi_quarter(1) == (4 & 3) && epi_quarter(2) == (1 & 3),
+              "each epilogue warp reads its own TMEM lane quarter");
 
 constexpr int kMmaM = 128;          // query rows padded to the full datapath
 constexpr int kMmaN = kPageTokens;  // 128 keys
@@ -199,7 +207,8 @@ __device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, Misc*
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // One request's 32 query rows into a TMEM query tile: lane r of the calling
-// warp (sub-partition 0) writes row r (128 bytes, 32 columns).
+// warp writes row r (128 bytes, 32 columns) into TMEM lane taddr.lane + r
+// (the warp's own lane quarter).
 __device__ __forceinline__ void write_query_tile(uint32_t taddr, const uint8_t* q_req, int lane) {
   uint32_t r[32];
   const uint4* src = reinterpret_cast<const uint4*>(q_req + lane * kHeadDim);
@@ -372,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     }
     // never leave with a copy in flight
     if (last >= 0) mbar_wait(&bars[kRawFull + lane], (uint32_t)(last / kStages) & 1u, nullptr);
-  } else if (warp >= kIssuerWarp0 && warp < kIssuerWarp0 + kPipe) {
+  } else if (issuer_of(warp) >= 0) {
     // ---------------- MMA issuers ----------------
     // The k-th page of issuer e waits for phase k of accumulator e's empty
     // barrier: phase 0 is the epilogue's first query-tile write, phase k its
@@ -381,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     // MMAs is warp-uniform, and one elected thread issues them: from a
     // single-thread branch a page's four MMAs took about twice as long to
     // issue.
-    const int e = warp - kIssuerWarp0;
+    const int e = issuer_of(warp);
     const uint32_t d = tmem + (uint32_t)e * kAccCols;
     const uint32_t qa = tmem + kQCol0 + (uint32_t)e * kQCols;
     bool issued_any = false;
@@ -412,9 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       __syncwarp();
       mbar_wait(&bars[kDrain + e], 0, nullptr);
     }
-  } else if (is_epi_warp(warp)) {
+  } else if (epi_of(warp) >= 0) {
     // ---------------- epilogue: lane = (slot, head) row ----------------
-    const int e = warp >> 2;  // pages i = e (mod 3), accumulator e
+    const int e = epi_of(warp);  // pages i = e (mod 3), accumulator e
+    const uint32_t quarter = (uint32_t)(32 * epi_quarter(e)) << 16;
     Cursor cur;
     cur.init(seq_lens, num_reqs, cap, b0, j0);
     cur.advance(e);
@@ -422,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     int prev_b = -1, own = -1;
     float qs = 0.f;
     bool neg = false;
-    const uint32_t acc = tmem + (uint32_t)e * kAccCols;
-    const uint32_t qa = tmem + kQCol0 + (uint32_t)e * kQCols;
+    const uint32_t acc = tmem + quarter + (uint32_t)e * kAccCols;
+    const uint32_t qa = tmem + quarter + kQCol0 + (uint32_t)e * kQCols;
     if (e < count) {
       write_query_tile(qa, q + (int64_t)cur.b * kQBytes, lane);
       tc_fence_before();
@@ -447,7 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       if (!__all_sync(0xFFFFFFFFu, ready)) break;  // the TMEM loads below are warp-wide
       tc_fence_after();
       const bool page_ok = valid_ring[i % kRing] != 0;
-      // one 32-column reduction per wait (it holds 32 registers of loaded values)
       // three rounds of loads in flight (32 + 16, 32 + 16, 32 columns): the
       // register budget holds 48 loaded values at a time
       float mx, mn = INFINITY;
