@@ -76,6 +76,22 @@ const char* idx_strerror(int code);
 int idx_have_qmul4(void);
 
 /*
+ * Wait budget of the tensor-core kernels (the decode scorer and the
+ * multi-token scorer).  Their warp roles hand pages to one another through
+ * shared-memory barriers; every such wait gives up after `polls` suspended
+ * polls of at most ~20 us each (spinning roles: polls * 1024 spins), records
+ * IDX_ST_TIMEOUT in the status word, and the CTA winds down: it stops taking
+ * pages, waits for its own copies and MMAs to land (those waits keep the
+ * default budget) and frees its tensor memory, so the stream and the context
+ * stay usable.  polls == 0 makes every pipeline wait a single test, so a
+ * launch times out as soon as one stage is not ready at once; that is for
+ * testing the timeout path.  The default is 100,000 (about 2 s).  The value
+ * is process-wide, read when a kernel is launched (a graph keeps the value
+ * it was captured with).  Returns the previous value.
+ */
+uint32_t idx_set_wait_limit(uint32_t polls);
+
+/*
  * Bytes of scratch workspace idx_topk16_select / idx_decode_step need for
  * `rows` rows of `width` columns (0 when rows fit one CTA each).  Rows longer
  * than 4,096 columns are split across CTAs whose local top-16s are merged
@@ -139,7 +155,8 @@ int idx_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, i
 /*
  * Exact top-16 per row ([PUBLISH] Changes; [CP] _page_keys).
  *
- *   scores        [rows, row_stride] float32, 4-byte aligned; columns [0, width).
+ *   scores        [rows, row_stride] float32, 4-byte aligned; columns [0, width);
+ *                 row_stride >= width (else IDX_E_BAD_SHAPE, whatever the row count).
  *   valid_n       [rows] int32 or NULL: row r ranks columns [0, min(valid_n[r], width));
  *                 NULL ranks all `width` columns.  Negative counts rank nothing.
  *   force_begin/end  columns in [force_begin, force_end) rank as +inf (empty if end <= begin).
@@ -170,9 +187,13 @@ int idx_topk16_select(const float* scores, int64_t row_stride, int32_t rows, int
  * a __device__ array inside the library: every GPU that loads the library
  * holds it until exit, every call shares it (it keeps the last call's
  * contents; nothing needs clearing), and calls that overlap on the GPU race
- * on it, so serialise them.  The first call on each device looks up the
- * array's address (cudaGetSymbolAddress, with that device current); make it
- * before any stream capture.  No allocation happens in any call.
+ * on it, so serialise them.  The first call in each CUDA context (for the
+ * runtime, each device's primary context) looks up the array's address
+ * (cudaGetSymbolAddress, with that device current) and caches it under the
+ * context's unique id; a new context -- after cudaDeviceReset, or a context
+ * the caller made current with the driver API -- is looked up afresh.  Make
+ * the first call in a context before any stream capture.  No allocation
+ * happens in any call.
  */
 #define IDX_NOALLOC_SCRATCH_BYTES (4u << 20)
 int idx_topk16_select_noalloc(const float* scores, int64_t row_stride, int32_t rows, int32_t width,

@@ -20,6 +20,8 @@ __all__ = [
     "idx_strerror",
     "idx_have_qmul4",
     "idx_workspace_bytes",
+    "idx_set_wait_limit",
+    "DEFAULT_WAIT_POLLS",
     "idx_dequant_nvfp4_pages",
     "idx_score_pages",
     "idx_topk16_select",
@@ -42,7 +44,8 @@ ST_BLOCK_OOR = 1
 ST_LEN_CLAMPED = 2
 ST_BAD_OUTPUT = 4
 ST_TIMEOUT = 8
-NOALLOC_SCRATCH_BYTES = 4 << 20  # scratch inside the library used by idx_topk16_select_noalloc
+NOALLOC_SCRATCH_BYTES = 4 << 20
+DEFAULT_WAIT_POLLS = 100_000  # pipeline-wait budget of the tensor-core kernels (about 2 s)  # scratch inside the library used by idx_topk16_select_noalloc
 
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -54,6 +57,7 @@ SYMBOLS = {
     "idx_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "idx_have_qmul4": (ctypes.c_int, []),
     "idx_workspace_bytes": (_sz, [_i32, _i32]),
+    "idx_set_wait_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
     "idx_dequant_nvfp4_pages": (ctypes.c_int, [_p, _i64, _p, _i64, _i32, _p, _p, _i32, _i32, _p, _i64, _p, _p]),
     "idx_score_pages": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p]),
     "idx_topk16_select": (ctypes.c_int, [_p, _i64, _i32, _i32, _p, _i32, _i32, _p, _p, _p, _sz, _p]),
@@ -104,6 +108,16 @@ def _row_stride(t) -> int:
     return t.stride(0) if t.shape[0] > 1 else t.shape[1]
 
 
+def _width(scores, width) -> int:
+    """Columns to rank: the tensor's width, or a narrower override (never wider)."""
+    if width is None:
+        return scores.shape[1]
+    width = int(width)
+    if width > scores.shape[-1]:
+        raise ValueError(f"width {width} exceeds the score tensor's {scores.shape[-1]} columns")
+    return width
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         import torch
@@ -132,6 +146,11 @@ def idx_workspace_bytes(rows: int, width: int) -> int:
     return int(load_library().idx_workspace_bytes(rows, width))
 
 
+def idx_set_wait_limit(polls: int) -> int:
+    """Set the tensor-core kernels' pipeline-wait budget (suspended polls); returns the previous one."""
+    return int(load_library().idx_set_wait_limit(int(polls)))
+
+
 def idx_dequant_nvfp4_pages(kv, block_table, num_pages, page_offsets, max_num_pages: int, out, status=None,
                             stream=None) -> int:
     """kv [num_blocks,128,72] u8; block_table [R, maxb] i32; out [>=sum,128,128] u8/e4m3."""
@@ -156,7 +175,7 @@ def idx_topk16_select(scores, out_idx, valid_n=None, force_begin: int = 0, force
     """scores [rows, >=width] f32 -> out_idx [rows,16] i32 (+ out_keys [rows,16] u64/i64)."""
     lib = load_library()
     rows = scores.shape[0]
-    width = scores.shape[1] if width is None else int(width)
+    width = _width(scores, width)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return _check("idx_topk16_select", lib.idx_topk16_select(
         _ptr(scores), _row_stride(scores), rows, width, _ptr(valid_n), int(force_begin), int(force_end), _ptr(out_idx),
@@ -169,7 +188,7 @@ def idx_topk16_select_noalloc(scores, out_idx, valid_n=None, force_begin: int = 
     is the library's own device array (at most NOALLOC_SCRATCH_BYTES)."""
     lib = load_library()
     rows = scores.shape[0]
-    width = scores.shape[1] if width is None else int(width)
+    width = _width(scores, width)
     return _check("idx_topk16_select_noalloc", lib.idx_topk16_select_noalloc(
         _ptr(scores), _row_stride(scores), rows, width, _ptr(valid_n), int(force_begin), int(force_end),
         _ptr(out_idx), _ptr(out_keys), _stream(stream)))

@@ -2,6 +2,7 @@
 // error text, device check, the decode scorer dispatch and the decode step.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -58,6 +59,12 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t ra
                 swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+std::atomic<uint32_t> g_wait_polls{kWaitPolls};
+}  // namespace
+
+uint32_t wait_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
+
 int launch_result() {
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) return IDX_OK;
@@ -110,6 +117,10 @@ extern "C" const char* idx_strerror(int code) {
     case IDX_E_DEVICE: return "the current device is not an sm_103 GPU";
     default: return "unknown libidx error";
   }
+}
+
+extern "C" uint32_t idx_set_wait_limit(uint32_t polls) {
+  return idx::g_wait_polls.exchange(polls, std::memory_order_relaxed);
 }
 
 extern "C" int idx_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,

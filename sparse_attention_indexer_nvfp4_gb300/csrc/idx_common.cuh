@@ -164,16 +164,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
   return ok != 0;
 }
 
-// Bounded wait: gives up after about kWaitLimit * kWaitHintNs (2 s) and
-// returns false.  A caller that gets false records IDX_ST_TIMEOUT and winds
-// its CTA down.  The abort flag (another role's timeout) is checked between
-// suspended polls.
+// Bounded wait: a suspended poll (parked until the phase completes or about
+// kWaitHintNs pass) repeated up to `polls` times, then false.  A caller that
+// gets false records IDX_ST_TIMEOUT and winds its CTA down.  The abort flag
+// (another role's timeout) is checked between polls.  polls == 0 tests the
+// phase once without parking.  Pipeline waits take their budget from the
+// launch (idx_set_wait_limit, default kWaitPolls, about 2 s); the waits that
+// drain a CTA's own copies and MMAs before it exits always use kWaitPolls,
+// because those complete by themselves within microseconds.
 constexpr uint32_t kWaitHintNs = 20000;
-constexpr uint32_t kWaitLimit = 100000;
+constexpr uint32_t kWaitPolls = 100000;
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_try_wait_nosuspend(uint64_t* bar, uint32_t parity);
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
+                                          uint32_t polls = kWaitPolls) {
+  if (polls == 0) return mbar_try_wait_nosuspend(bar, parity);
   if (mbar_try_wait(bar, parity, kWaitHintNs)) return true;
-  for (uint32_t i = 1; i < kWaitLimit; ++i) {
+  for (uint32_t i = 1; i < polls; ++i) {
     if (abort_flag != nullptr && *abort_flag) return false;
     if (mbar_try_wait(bar, parity, kWaitHintNs)) return true;
   }
@@ -200,8 +208,8 @@ __device__ __forceinline__ void mbar_test2(uint64_t* bar_a, uint32_t parity_a, u
 
 // Spinning variant for roles on a pipeline's critical loop, where waking a
 // suspended warp costs more than the wait: polls without a suspend hint,
-// checks the abort flag every 256 polls, gives up after about 2^26 polls
-// (a few seconds).
+// checks the abort flag every 256 polls, gives up after `polls` * 1024 polls
+// (about 2^26, a few seconds, at the default budget; one poll at 0).
 __device__ __forceinline__ bool mbar_try_wait_nosuspend(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -212,8 +220,10 @@ __device__ __forceinline__ bool mbar_try_wait_nosuspend(uint64_t* bar, uint32_t 
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const volatile int* abort_flag) {
-  for (uint32_t i = 0; i < (1u << 26); ++i) {
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
+                                          uint32_t polls = kWaitPolls) {
+  const uint64_t spins = polls == 0 ? 1ull : (uint64_t)polls << 10;
+  for (uint64_t i = 0; i < spins; ++i) {
     if (mbar_try_wait_nosuspend(bar, parity)) return true;
     if ((i & 255u) == 255u && abort_flag != nullptr && *abort_flag) return false;
   }

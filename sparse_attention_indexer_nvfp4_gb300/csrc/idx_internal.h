@@ -17,6 +17,10 @@ int check_device();
 // Map the launch's cudaGetLastError() to a return code.
 int launch_result();
 
+// Wait budget of the tensor-core kernels' pipeline waits, in suspended polls
+// (idx_set_wait_limit; passed to every launch).
+uint32_t wait_polls();
+
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // cuTensorMapEncodeTiled, reached through the runtime's driver entry point

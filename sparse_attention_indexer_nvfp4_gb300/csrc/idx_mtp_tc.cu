@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
                                                       const float* __restrict__ k_scale, int64_t num_blocks,
                                                       const int32_t* __restrict__ bt, int64_t bt_stride,
                                                       ReqShape shape, int32_t max_keys, float* __restrict__ out,
-                                                      int32_t* status) {
+                                                      int32_t* status, uint32_t wait_polls) {
   pdl_enter();  // before any global-memory access
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
         if (lane == 0) {
           if (cur.r != pr || cur.tt != ptt) {
             const int qb = (qord + 1) % kQBufsM;
-            if (timed_wait_flag(&bars[kQEmpty + qb], ((uint32_t)((qord + 1) / kQBufsM) & 1u) ^ 1u, abort_flag, status)) {
+            if (timed_wait_flag(&bars[kQEmpty + qb], ((uint32_t)((qord + 1) / kQBufsM) & 1u) ^ 1u, abort_flag, status, wait_polls)) {
               pr = cur.r, ptt = cur.tt;
               ++qord;
               const int t0 = shape.tok0(cur.r) + kTokTile * cur.tt;
@@ -238,8 +238,8 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
           bool k_free = false, ks_free = false;
           if (ok) {
             mbar_test2(&bars[kKEmpty + stage], p_k, &bars[kKsEmpty + ks], p_ks, k_free, ks_free);
-            if (!k_free) k_free = timed_wait_flag(&bars[kKEmpty + stage], p_k, abort_flag, status);
-            if (k_free && !ks_free) ks_free = timed_wait_flag(&bars[kKsEmpty + ks], p_ks, abort_flag, status);
+            if (!k_free) k_free = timed_wait_flag(&bars[kKEmpty + stage], p_k, abort_flag, status, wait_polls);
+            if (k_free && !ks_free) ks_free = timed_wait_flag(&bars[kKsEmpty + ks], p_ks, abort_flag, status, wait_polls);
             ok = k_free && ks_free;
           }
           if (ok) {
@@ -286,11 +286,11 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
           pr = cur.r, ptt = cur.tt;
           if (qord >= 0) mma_commit(&bars[kQEmpty + qord % kQBufsM]);  // the previous query tile is done
           ++qord;
-          if (!spin_wait_flag(&bars[kQFull + qord % kQBufsM], (uint32_t)(qord / kQBufsM) & 1u, abort_flag, status)) break;
+          if (!spin_wait_flag(&bars[kQFull + qord % kQBufsM], (uint32_t)(qord / kQBufsM) & 1u, abort_flag, status, wait_polls)) break;
         }
         const int stage = i % kStages, a = i & 1;
-        if (!spin_wait_flag(&bars[kKFull + stage], (uint32_t)(i / kStages) & 1u, abort_flag, status)) break;
-        if (!spin_wait_flag(&bars[kAEmpty + a], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, status)) break;
+        if (!spin_wait_flag(&bars[kKFull + stage], (uint32_t)(i / kStages) & 1u, abort_flag, status, wait_polls)) break;
+        if (!spin_wait_flag(&bars[kAEmpty + a], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, status, wait_polls)) break;
         tc_fence_after();
         const uint64_t adesc = sw128_desc(sbase + kOffKm + stage * kKTileBytes);
         const uint64_t bdesc = sw128_desc(sbase + kOffQm + (qord % kQBufsM) * kQTileBytes);
@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
         const uint32_t p_ks = (uint32_t)(i / kKsSlots) & 1u, p_acc = (uint32_t)(i >> 1) & 1u;
         bool ks_ok, acc_ok;
         mbar_test2(&bars[kKsFull + slot], p_ks, &bars[kAFull + set], p_acc, ks_ok, acc_ok);
-        if (!ks_ok) ks_ok = timed_wait_flag(&bars[kKsFull + slot], p_ks, abort_flag, status);
-        if (ks_ok && !acc_ok) acc_ok = timed_wait_flag(&bars[kAFull + set], p_acc, abort_flag, status);
+        if (!ks_ok) ks_ok = timed_wait_flag(&bars[kKsFull + slot], p_ks, abort_flag, status, wait_polls);
+        if (ks_ok && !acc_ok) acc_ok = timed_wait_flag(&bars[kAFull + set], p_acc, abort_flag, status, wait_polls);
         if (!__all_sync(0xFFFFFFFFu, ks_ok && acc_ok)) break;
       }
       tc_fence_after();
@@ -425,7 +425,7 @@ int launch_mtp_tc(const uint8_t* q, const float* q_scale, int32_t num_tokens, co
   // two CTAs per SM: 256 TMEM columns and ~100 KB of shared memory each
   const int grid = 2 * g_sms_m[dev];
   launch_pdl(k_mtp_tc, dim3(grid), dim3(kThreadsM), kSmemM, stream, kmap, qmap, q_scale, k_scale, num_blocks, bt, bt_stride, sh, max_keys,
-                                                 out, status);
+                                                 out, status, wait_polls());
   return launch_result();
 }
 

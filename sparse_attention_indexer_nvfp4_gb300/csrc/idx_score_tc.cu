@@ -51,9 +51,10 @@
 // writes 9 KB, the dequant reads 9 KB of codes and 8 KB of table rows and
 // writes a 16 KB K tile, and the tensor core reads that tile.  Keeping the
 // query operand in TMEM spares another 16 KB per page (the MMA reads all 128
-// rows of A at M=128, though only 32 carry queries; rows 32-127 of a query
-// tile hold whatever the TMEM held and only produce accumulator rows that
-// nothing reads).
+// rows of A at M=128, though only 32 carry queries: the 32 rows of query tile
+// e in lane quarter epi_quarter(e).  The tile's other 96 rows are never
+// written and hold whatever the TMEM held; the accumulator rows they produce
+// are never read, since epilogue warp e reads its own lane quarter only).
 // q_scale is applied after the max: RN multiplication is monotone, so
 // qs * max_t x_t == max_t RN(qs * x_t) for qs >= 0 (and with min for qs < 0).
 //
@@ -195,8 +196,9 @@ __device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, uint32_t after)
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)), "r"(after) : "memory");
 }
 
-__device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, Misc* misc, int32_t* status) {
-  if (mbar_wait(bar, parity, &misc->abort_flag)) return true;
+__device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, Misc* misc, int32_t* status,
+                                           uint32_t polls) {
+  if (mbar_wait(bar, parity, &misc->abort_flag, polls)) return true;
   if (!misc->abort_flag) {
     misc->abort_flag = 1;
     report(status, IDX_ST_TIMEOUT);
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     const uint8_t* __restrict__ q, const float* __restrict__ q_scale, const uint8_t* __restrict__ kv,
     int64_t num_blocks, const int32_t* __restrict__ bt, int64_t bt_stride, int32_t max_blocks,
     const int32_t* __restrict__ seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
-    float* __restrict__ scores, int32_t* status) {
+    float* __restrict__ scores, int32_t* status, uint32_t wait_polls) {
   pdl_enter();  // before any global-memory access
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -400,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       const uint32_t p_kt = (uint32_t)(i / kKtPeriod) & 1u, p_acc = (uint32_t)(i / kPipe) & 1u;
       bool kt_ok, acc_ok;
       mbar_test2(kt_full, p_kt, &bars[kAccEmpty + e], p_acc, kt_ok, acc_ok);
-      if (!kt_ok) kt_ok = timed_wait(kt_full, p_kt, misc, status);
-      if (kt_ok && !acc_ok) acc_ok = timed_wait(&bars[kAccEmpty + e], p_acc, misc, status);
+      if (!kt_ok) kt_ok = timed_wait(kt_full, p_kt, misc, status, wait_polls);
+      if (kt_ok && !acc_ok) acc_ok = timed_wait(&bars[kAccEmpty + e], p_acc, misc, status, wait_polls);
       if (!__all_sync(0xFFFFFFFFu, kt_ok && acc_ok)) break;
       tc_fence_after();
       if (elect_one()) {
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
         neg = __any_sync(0xFFFFFFFFu, !(qs >= 0.f));
         own = iq >= 0 ? floor_div_page(seq_lens[b] - query_len + iq) : -1;
       }
-      const bool ready = timed_wait(&bars[kAccFull + e], (uint32_t)(i / kPipe) & 1u, misc, status);
+      const bool ready = timed_wait(&bars[kAccFull + e], (uint32_t)(i / kPipe) & 1u, misc, status, wait_polls);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;  // the TMEM loads below are warp-wide
       tc_fence_after();
       const bool page_ok = valid_ring[i % kRing] != 0;
@@ -511,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
         const uint32_t p_kt = ((uint32_t)(i / (kGroups * kGroupTiles)) & 1u) ^ 1u;
         bool raw_ok, kt_ok;
         mbar_test2(&bars[kRawFull + stage], p_raw, &bars[kKtEmpty + tile], p_kt, raw_ok, kt_ok);
-        if (!raw_ok) raw_ok = timed_wait(&bars[kRawFull + stage], p_raw, misc, status);
-        if (raw_ok && !kt_ok) kt_ok = timed_wait(&bars[kKtEmpty + tile], p_kt, misc, status);
+        if (!raw_ok) raw_ok = timed_wait(&bars[kRawFull + stage], p_raw, misc, status, wait_polls);
+        if (raw_ok && !kt_ok) kt_ok = timed_wait(&bars[kKtEmpty + tile], p_kt, misc, status, wait_polls);
         if (!__all_sync(0xFFFFFFFFu, raw_ok && kt_ok)) break;  // the warp stays converged for its ballot
       }
       // codes and scales into registers, then the raw stage goes back to the
@@ -586,7 +588,7 @@ int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, i
   // one CTA per SM: each CTA holds all 512 TMEM columns of its SM
   const int grid = (int)std::min<int64_t>((int64_t)g_sms[dev], upper);
   launch_pdl(k_score_decode, dim3(grid), dim3(kThreads), kSmemBytes, stream, q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks,
-                                                          seq_lens, num_reqs, query_len, width, scores, status);
+                                                          seq_lens, num_reqs, query_len, width, scores, status, wait_polls());
   return launch_result();
 }
 

@@ -138,8 +138,8 @@ __device__ __forceinline__ bool elect_one() {
 
 // Bounded waits that record a timeout in `status` and raise the CTA's abort flag.
 __device__ __forceinline__ bool timed_wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                int32_t* status) {
-  if (mbar_wait(bar, parity, abort_flag)) return true;
+                                                int32_t* status, uint32_t polls) {
+  if (mbar_wait(bar, parity, abort_flag, polls)) return true;
   if (!*abort_flag) {
     *abort_flag = 1;
     report(status, IDX_ST_TIMEOUT);
@@ -148,8 +148,8 @@ __device__ __forceinline__ bool timed_wait_flag(uint64_t* bar, uint32_t parity, 
 }
 
 __device__ __forceinline__ bool spin_wait_flag(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                               int32_t* status) {
-  if (mbar_spin(bar, parity, abort_flag)) return true;
+                                               int32_t* status, uint32_t polls) {
+  if (mbar_spin(bar, parity, abort_flag, polls)) return true;
   if (!*abort_flag) {
     *abort_flag = 1;
     report(status, IDX_ST_TIMEOUT);

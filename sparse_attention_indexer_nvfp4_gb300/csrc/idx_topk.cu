@@ -450,7 +450,7 @@ extern "C" int idx_topk16_select(const float* scores, int64_t row_stride, int32_
   if (rows == 0) return IDX_OK;
   if (!out_idx) return IDX_E_NULL_PTR;
   if (width > 0 && !scores) return IDX_E_NULL_PTR;
-  if (width > 0 && row_stride < width && rows > 1) return IDX_E_BAD_SHAPE;
+  if (width > 0 && row_stride < width) return IDX_E_BAD_SHAPE;
   if (!aligned(scores, 4) || !aligned(out_idx, 4) || !aligned(out_keys, 8) || !aligned(valid_n, 4) ||
       !aligned(workspace, 8))
     return IDX_E_MISALIGNED;

@@ -17,9 +17,14 @@
 // it and must be serialised by the caller.
 //
 // Host code cannot use the array's name as a device address, so the first
-// call on each device (with that device current) looks the address up with
-// cudaGetSymbolAddress and caches it; make that first call before any
-// stream capture.
+// call in each CUDA context looks the address up with cudaGetSymbolAddress
+// (with the context's device current) and caches it under the context's
+// unique id (cuCtxGetId: ids are never reused, so a context created after a
+// device reset, or one the caller made current through the driver API, gets
+// its own lookup instead of a stale address).  Make the first call in a
+// context before any stream capture.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "idx_common.cuh"
@@ -31,23 +36,59 @@ namespace {
 static __device__ __align__(256) uint8_t g_noalloc_scratch[IDX_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDev = 64;
-void* g_scratch_ptr[kMaxDev];
+struct Cached {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+Cached g_scratch[kMaxDev];
 std::mutex g_scratch_mu;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
 
-// Device address of the scratch array on the current device (set up once per device).
+template <typename F>
+bool driver_fn(const char* name, int version, F* out) {
+  cudaDriverEntryPointQueryResult qr;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &qr) != cudaSuccess ||
+      qr != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  *out = reinterpret_cast<F>(fn);
+  return true;
+}
+
+// Unique id of the current context (0 when none is current yet).
+bool current_ctx_id(unsigned long long* id) {
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return ctx == nullptr || g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return IDX_E_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-      (void)cudaGetLastError();
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr) {
+    if (!driver_fn("cuCtxGetCurrent", 4000, &g_ctx_current) || !driver_fn("cuCtxGetId", 12000, &g_ctx_id)) {
+      g_ctx_current = nullptr;
       return IDX_E_CUDA;
     }
-    g_scratch_ptr[dev] = p;
   }
-  *out = g_scratch_ptr[dev];
+  unsigned long long id = 0;
+  if (!current_ctx_id(&id)) return IDX_E_CUDA;
+  if (id != 0 && g_scratch[dev].ptr != nullptr && g_scratch[dev].ctx_id == id) {
+    *out = g_scratch[dev].ptr;
+    return IDX_OK;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();
+    return IDX_E_CUDA;
+  }
+  if (id == 0 && !current_ctx_id(&id)) return IDX_E_CUDA;  // the lookup made the primary context current
+  g_scratch[dev] = Cached{id, p};
+  *out = p;
   return IDX_OK;
 }
 
@@ -62,7 +103,7 @@ extern "C" int idx_topk16_select_noalloc(const float* scores, int64_t row_stride
   if (rows == 0) return IDX_OK;
   if (!out_idx) return IDX_E_NULL_PTR;
   if (width > 0 && !scores) return IDX_E_NULL_PTR;
-  if (width > 0 && row_stride < width && rows > 1) return IDX_E_BAD_SHAPE;
+  if (width > 0 && row_stride < width) return IDX_E_BAD_SHAPE;
   if (!aligned(scores, 4) || !aligned(out_idx, 4) || !aligned(out_keys, 8) || !aligned(valid_n, 4))
     return IDX_E_MISALIGNED;
   if (topk_workspace_bytes(rows, width) > (size_t)IDX_NOALLOC_SCRATCH_BYTES) return IDX_E_TOO_LARGE;

@@ -68,3 +68,21 @@ def selection_within_tolerance(gpu_out: np.ndarray, ref_out: np.ndarray, ref_sco
                 tol = 2 * float(ref_bound[b, row].max())
                 assert len(gs) == len(rs) and all(abs(x - y) <= tol for x, y in zip(gs, rs)), (b, i, h)
     return differ
+
+
+def topk_within_tolerance(gpu_idx: np.ndarray, ref_idx: np.ndarray, ref_scores: np.ndarray,
+                          ref_bound: np.ndarray) -> int:
+    """Top-16 rows of the GPU's scores vs the oracle's own: a row may differ
+    only where the oracle scores of the two selections agree within twice the
+    row's tolerance, rank by rank.  Returns the number of rows that differ."""
+    differ = 0
+    for r in range(gpu_idx.shape[0]):
+        g, w = gpu_idx[r], ref_idx[r]
+        if np.array_equal(g, w):
+            continue
+        differ += 1
+        gs = sorted((float(ref_scores[r, c]) for c in g if c >= 0), reverse=True)
+        ws = sorted((float(ref_scores[r, c]) for c in w if c >= 0), reverse=True)
+        tol = 2 * float(np.nanmax(ref_bound[r]))
+        assert len(gs) == len(ws) and all(abs(x - y) <= tol for x, y in zip(gs, ws)), r
+    return differ

@@ -67,6 +67,30 @@ def test_error_codes_and_strings(built):
     assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 5000, 16, 16, None, 0, None, None) == E_WS
 
 
+def test_wait_limit_setter_returns_the_previous_budget(built):
+    prev = built.idx_set_wait_limit(7)
+    assert prev == built.DEFAULT_WAIT_POLLS
+    assert built.idx_set_wait_limit(prev) == 7
+    assert built.idx_set_wait_limit(prev) == prev
+
+
+def test_binding_rejects_a_width_past_the_tensor(built):
+    import torch
+
+    scores = torch.zeros((1, 40), dtype=torch.float32)
+    idx = torch.zeros((1, 16), dtype=torch.int32)
+    for fn in (built.idx_topk16_select, built.idx_topk16_select_noalloc):
+        with pytest.raises(ValueError):
+            fn(scores, idx, width=41)
+
+
+def test_one_row_stride_is_checked(built):
+    lib = built.load_library()
+    # a single row whose stride is below the width reads past the row: rejected
+    assert lib.idx_topk16_select(16, 10, 1, 100, None, 0, 0, 16, None, None, 0, None) == -2
+    assert lib.idx_topk16_select_noalloc(16, 10, 1, 100, None, 0, 0, 16, None, None) == -2
+
+
 def test_workspace_sizing(built):
     # one CTA covers up to 4,096 columns; wider rows split across CTAs
     assert built.idx_workspace_bytes(100, 1) == 0

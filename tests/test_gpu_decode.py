@@ -159,49 +159,49 @@ def test_signed_and_special_scales(lib):
     _check_step(wl, s, out)
 
 
-@pytest.mark.slow
-def test_full_batched_decode_sampled(lib):
-    """64 requests, seq_len U[8K, 168K], 1,344-column rows, 1% duplicated pages:
-    the full selection bit-exact on the GPU's own scores, sampled pages' scores
-    against the oracle, and the end-to-end rows of sampled requests."""
-    wl = W.batched_decode()
-    s, out, st = _step(lib, wl)
-    assert st == 0
+def _check_full(wl, s, out):
+    """Every written score of a full-size workload against the oracle (on all
+    host cores), the untouched pattern, the selection bit for bit on the
+    GPU's own scores, and the end-to-end rows against the oracle's: the
+    number of rows that differ at a near-tie is returned (expected 0)."""
+    import oracle_pool
+
+    ref, written, bound, st_ref = oracle_pool.decode_scores_full(wl, 8)
+    info = check_scores(s, ref, written, bound)
     sel, _, _ = decode_step(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"], 8, wl["width"],
                             wl["max_blocks"], scores=s)
     assert np.array_equal(out, sel)
-    rng = np.random.default_rng(1)
-    pairs = []
-    for b in range(64):
-        n = (int(wl["seq_lens"][b]) - 1) // 128
-        for j in rng.integers(0, n, size=3):
-            pairs.append((b, int(j)))
-    ref, written, bound, _ = decode_scores(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"], 8,
-                                           wl["width"], wl["max_blocks"], pages=pairs)
-    mask = written
-    err = np.abs(s[mask].astype(np.float64) - ref[mask].astype(np.float64))
-    assert (err <= bound[mask]).all()
-    # untouched columns: everything at or past each row's own page
-    for b in range(64):
-        own = (int(wl["seq_lens"][b]) - 8) // 128
-        assert (s[b, :, own + 1:].view(np.int32) == 0x7FBADBAD).all()
+    ref_out, _, _ = decode_step(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"], 8, wl["width"],
+                                wl["max_blocks"], scores=ref)
+    info["near_tie_rows"] = selection_within_tolerance(out, ref_out, ref, bound, 8)
+    info["rows"] = int(out.shape[0] * out.shape[1] * out.shape[2])
+    return info, st_ref
+
+
+@pytest.mark.slow
+def test_full_batched_decode(lib):
+    """64 requests, seq_len U[8K, 168K], 1,344-column rows, 1% duplicated pages:
+    all 47,603 pages' scores against the oracle, the selection bit for bit,
+    and no end-to-end row differing from the oracle's (near-ties: 0)."""
+    wl = W.batched_decode()
+    s, out, st = _step(lib, wl)
+    info, st_ref = _check_full(wl, s, out)
+    print(f"\nbatched decode: {info}")
+    assert st == st_ref == 0
+    assert info["near_tie_rows"] == 0
 
 
 @pytest.mark.slow
 def test_long_context_decode(lib):
-    """16 requests x 500,000 tokens (3,906 pages per row): split rows merged exactly."""
+    """16 requests x 500,000 tokens (3,906 pages per row, split rows merged):
+    every page's scores against the oracle, the selection bit for bit, and no
+    end-to-end row differing from the oracle's."""
     wl = W.long_context()
     s, out, st = _step(lib, wl)
-    assert st == 0
-    sel, _, _ = decode_step(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"], 8, wl["width"],
-                            wl["max_blocks"], scores=s)
-    assert np.array_equal(out, sel)
-    rng = np.random.default_rng(2)
-    pairs = [(int(b), int(j)) for b, j in zip(rng.integers(0, 16, 40), rng.integers(0, 3906, 40))]
-    ref, written, bound, _ = decode_scores(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"], 8,
-                                           wl["width"], wl["max_blocks"], pages=pairs)
-    err = np.abs(s[written].astype(np.float64) - ref[written].astype(np.float64))
-    assert (err <= bound[written]).all()
+    info, st_ref = _check_full(wl, s, out)
+    print(f"\nlong context: {info}")
+    assert st == st_ref == 0
+    assert info["near_tie_rows"] == 0
 
 
 def test_many_short_requests_and_repeatability(lib):

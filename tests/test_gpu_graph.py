@@ -80,3 +80,24 @@ def test_mtp_step_graph_replay(lib):
     assert torch.equal(o.view(torch.int32), eager_o.view(torch.int32))
     assert torch.equal(idx, eager_idx)
     assert (idx >= 0).all()
+
+
+def test_no_alloc_selector_graph_replay(lib):
+    """The selector that allocates nothing, captured after one call outside
+    capture (its first call in the context looks up the scratch address):
+    replays with new scores copied in match the workspace entry point."""
+    data = [W.topk_rows(905, 96, 9000), W.topk_rows(906, 96, 9000)]
+    scores = dev(data[0]["scores"])
+    idx = torch.full((96, 16), -7, dtype=torch.int32, device="cuda")
+    assert lib.idx_workspace_bytes(96, 9000) > 0  # rows split across CTAs: the scratch is used
+    g = _capture(lambda: lib.idx_topk16_select_noalloc(scores, idx))
+    wsb = lib.idx_workspace_bytes(96, 9000)
+    ws = torch.empty(wsb // 8, dtype=torch.int64, device="cuda")
+    want = torch.empty_like(idx)
+    for d in data + data[:1]:
+        scores.copy_(dev(d["scores"]))
+        idx.fill_(-7)
+        g.replay()
+        lib.idx_topk16_select(scores, want, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, want)
