@@ -10,10 +10,17 @@
 // One persistent CTA per SM takes the contiguous slice [P*c/G, P*(c+1)/G) of
 // all (request, page) pairs.  Pages flow through a pipeline of warp roles:
 //
-//   producer (1 warp)   raw NVFP4 page -> 8-stage shared-memory ring, one
-//                       9,216-byte bulk copy per page (a 72-byte row is not a
-//                       legal TMA box); lane s refills stage s as soon as
-//                       it is free, polling its own empty barrier;
+//   producer (1 warp)   walks the slice 32 pages at a time and writes one
+//                       record per page into a shared-memory ring (request,
+//                       page, block id, whether the request has a negative
+//                       q_scale, and the request whose query rows replace an
+//                       accumulator's query tile after the page), so that no
+//                       other role does (request, page) arithmetic or loads
+//                       the block table; then raw NVFP4 page -> 8-stage
+//                       shared-memory ring, one 9,216-byte bulk copy per page
+//                       (a 72-byte row is not a legal TMA box); lane s
+//                       refills stage s as soon as it is free, polling its
+//                       own empty barrier;
 //   dequant (16 warps)  4 groups of 4 warps, group g takes pages i = g (mod 4)
 //                       and owns two K tiles (one filled while the MMA reads
 //                       the other): the page becomes a 128B-swizzled
@@ -32,20 +39,33 @@
 //                       tcgen05.mma kind::f8f6f4, M=128 x N=128 (keys) x K=128
 //                       (four K=32 steps) into TMEM accumulator e.  A (the
 //                       request's query rows) is read from TMEM, so the only
-//                       shared-memory operand is the page's K tile;
+//                       shared-memory operand is the page's K tile.  Then,
+//                       while that MMA runs, it stores page i - 6's scores:
+//                       lane = (slot, head) row, q_scale applied (after the
+//                       max, or the min for a negative scale), NaN for a bad
+//                       block id, only pages below the row's own page;
 //   epilogue (3 warps)  warp e takes pages i = e (mod 3) and accumulator e,
 //                       reduces each (slot, head) row's 128 key scores with
-//                       tcgen05.ld.red (the load takes the max), applies q_scale
-//                       and stores the score.  It also owns issuer e's query
-//                       tile in TMEM: it writes the request's 32 query rows
-//                       before the first page and rewrites them when the
-//                       request changes, after the accumulator-full wait (the
-//                       previous MMA has read them) and before releasing the
-//                       accumulator to the issuer.  The query rows (and so the
-//                       accumulator's rows of scores) sit in the TMEM lane
-//                       quarter of the epilogue warp's sub-partition: lanes
-//                       0-31 for accumulators 0 and 1 (warps 0 and 4), lanes
-//                       32-63 for accumulator 2 (warp 1).
+//                       tcgen05.ld.red (the load takes the max, and the min
+//                       too when the request has a negative q_scale), releases
+//                       the accumulator, then writes the 32 row maxima to one
+//                       of accumulator e's three score slots (off the
+//                       round trip: a shared-memory store there costs ~200
+//                       cycles with the dequant warps' traffic in the same
+//                       queue); its next release, of page i + 3, tells issuer
+//                       e that the slot of page i is filled.  It also owns issuer
+//                       e's query tile in TMEM: it writes the request's 32
+//                       query rows before the first page and rewrites them
+//                       when the page's record says so, after the
+//                       accumulator-full wait (the previous MMA has read them)
+//                       and before releasing the accumulator to the issuer.
+//                       The query rows (and so the accumulator's rows of
+//                       scores) sit in the TMEM lane quarter of the epilogue
+//                       warp's sub-partition: lanes 0-31 for accumulators 0
+//                       and 1 (warps 0 and 4), lanes 32-63 for accumulator 2
+//                       (warp 1).  This warp's chain (wait, reduce, release)
+//                       is the accumulator's round trip, so it carries nothing
+//                       else.
 //
 // Shared memory is the resource this kernel spends per page: the bulk copy
 // writes 9 KB, the dequant reads 9 KB of codes and 8 KB of table rows and
@@ -76,12 +96,11 @@ constexpr int kKTiles = kGroups * kGroupTiles;
 constexpr int kGroupWarps = 4;  // each warp of a group takes a quarter page (32 keys)
 constexpr int kPipe = 3;        // accumulators, MMA issuers and epilogue warps; issuer/epilogue e own accumulator e
 constexpr int kProducerWarp = 2;
+constexpr int kFirstDequantWarp = 7;
 constexpr int kThreads = 23 * 32;
 constexpr uint32_t kProducerIdleLimit = 1u << 24;  // idle polls (~64 ns back-off each) before a timeout
 // Warp roles by sub-partition (warp w runs on sub-partition w % 4; at most
-// six warps on one, so 80 registers per thread -- with seven on one the cap
-// was 72 and the epilogue's page bookkeeping spilled to local memory, inside
-// the accumulator's round trip):
+// six warps on one, so 80 registers per thread):
 //   0: epilogue 0 (warp 0), epilogue 1 (4); dequant 8, 12, 16, 20
 //   1: epilogue 2 (1); issuer 0 (5); dequant 9, 13, 17, 21
 //   2: producer (2); issuer 1 (6); dequant 10, 14, 18, 22
@@ -91,11 +110,13 @@ constexpr uint32_t kProducerIdleLimit = 1u << 24;  // idle polls (~64 ns back-of
 __host__ __device__ constexpr int epi_of(int w) { return w == 0 ? 0 : w == 4 ? 1 : w == 1 ? 2 : -1; }
 __host__ __device__ constexpr int epi_quarter(int e) { return e == 2 ? 1 : 0; }
 __host__ __device__ constexpr int issuer_of(int w) { return w == 5 ? 0 : w == 6 ? 1 : w == 3 ? 2 : -1; }
-__host__ __device__ constexpr bool is_dequant_warp(int w) { return w >= 7 && w < 23; }
+__host__ __device__ constexpr bool is_dequant_warp(int w) { return w >= kFirstDequantWarp && w < kThreads / 32; }
 // group of dequant warp w (its in-group index is its sub-partition w % 4)
-__host__ __device__ constexpr int dequant_group(int w) { return (w - 7) >> 2; }
+__host__ __device__ constexpr int dequant_group(int w) { return (w - kFirstDequantWarp) >> 2; }
 static_assert(epi_quarter(0) == (0 & 3) && epi_quarter(1) == (4 & 3) && epi_quarter(2) == (1 & 3),
               "each epilogue warp reads its own TMEM lane quarter");
+static_assert(kThreads / 32 - kFirstDequantWarp == kGroups * kGroupWarps,
+              "four consecutive warps per dequant group: one on every sub-partition");
 
 constexpr int kMmaM = 128;          // query rows padded to the full datapath
 constexpr int kMmaN = kPageTokens;  // 128 keys
@@ -109,20 +130,43 @@ static_assert(kQCol0 + kPipe * kQCols <= kTmemCols, "accumulators and query tile
 constexpr int kKTile = kPageTokens * kHeadDim;  // 16384
 constexpr int kQBytes = kRows * kHeadDim;       // 4096: one request's 32 query rows
 constexpr int kLutCopies = 8;  // lane & 7 picks a copy
-// Page validity ring, written by the producer, read by the dequant group and
-// the epilogue of each page.  The producer writes the slot of page i + 64
-// only after the dequant of page i + 56 has loaded its codes (raw stage
-// reuse), which waited for the MMA of page i + 48 to read its K tile (tile
-// reuse), which waited for the epilogue of page i + 45 (accumulator reuse;
-// 48 is a multiple of 3, so that is page i's epilogue warp, which works in
-// order) and for the dequant of page i + 48 (page i's group, in order).  So
-// both readers of slot i are done before it is rewritten.
-constexpr int kRing = 64;
+// Page records, written by the producer 32 at a time, read by the producer
+// (block id), the dequant group (validity), the epilogue (flags) and the
+// issuer that stores the page's scores (request, page, validity), which is
+// the last reader: issuer e stores page i when it issues page i + 6.  Each issuer publishes the last page it stored; the
+// producer writes the records of pages [g, g + 32) only once every issuer has
+// stored every page below g + 32 - kRecs, so no record is rewritten before
+// all its readers are done.  Pages in flight between the stores and the
+// copies are at most the raw stages, the K tiles and two rounds of the
+// accumulators (~25),
+// well below kRecs - 32, so the condition never holds the pipeline back.
+constexpr int kRecs = 128;
+constexpr int kRecChunk = 32;
+constexpr int kRecNeg = 1 << 30;        // flags: the request has a q_scale that is not >= 0
+constexpr int kRecQueryMask = 0xFFFFF;  // flags: (request whose rows replace the tile after this page) + 1, 0 = none
+struct __align__(16) PageRec {
+  int b, j, blk, flags;
+};
+// Score slots, three per accumulator (page i in slot (i / 3) % 3 of
+// accumulator i % 3): the 32 row maxima, then the 32 row minima (written only
+// for a request with a negative q_scale).  The epilogue writes page i's slot
+// after releasing page i and before releasing page i + 3; issuer e reads it
+// after that second release (its wait for page i + 6) and before it issues
+// page i + 9, whose epilogue is the next to write that slot.  After its last
+// page the epilogue arrives on a barrier of its own (slot done) once that
+// page's slot is written.  (An extra phase of the accumulator's empty barrier
+// would not do: the issuer could then be two phases behind, and a parity wait
+// cannot tell those apart.)
+constexpr int kSlotsPerAcc = 3;
+constexpr int kScoreSlots = kSlotsPerAcc * kPipe;
+__host__ __device__ constexpr int score_slot(int i) { return (i % kPipe) * kSlotsPerAcc + (i / kPipe) % kSlotsPerAcc; }
+constexpr int kReqCache = 256;  // page counts of the first kReqCache requests, cached in shared memory
 constexpr int kOffK = 0;
 constexpr int kOffRaw = kOffK + kKTiles * kKTile;
 constexpr int kOffLut = kOffRaw + kStages * kPageBytes;
-constexpr int kOffValid = kOffLut + 256 * 8 * kLutCopies;
-constexpr int kOffBar = kOffValid + kRing * 4;
+constexpr int kOffRec = kOffLut + 256 * 8 * kLutCopies;
+constexpr int kOffScore = kOffRec + kRecs * (int)sizeof(PageRec);
+constexpr int kOffBar = kOffScore + kScoreSlots * 2 * kRows * 4;
 // K-tile full barriers are kept per (tile, issuer): pages of one tile are 8
 // apart and their issuers cycle through all three, so a single barrier per
 // tile would have three waiters, and a waiter one phase behind could pass on
@@ -131,12 +175,15 @@ constexpr int kOffBar = kOffValid + kRing * 4;
 // in order (parity (i / 24) & 1).
 constexpr int kKtPeriod = kKTiles * kPipe;  // 24
 enum Bars { kRawFull = 0, kRawEmpty = kStages, kKtFull = 2 * kStages, kKtEmpty = kKtFull + kKTiles * kPipe, kAccFull = kKtEmpty + kKTiles,
-            kAccEmpty = kAccFull + kPipe, kDrain = kAccEmpty + kPipe, kNumBars = kDrain + kPipe };
+            kAccEmpty = kAccFull + kPipe, kDrain = kAccEmpty + kPipe, kSlotDone = kDrain + kPipe,
+            kNumBars = kSlotDone + kPipe };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffReqPages = kOffMisc + 64;  // [kThreads] int: pages of the first kThreads requests
-constexpr int kSmemBytes = kOffReqPages + kThreads * 4 + 1024;  // + slack to align the base to 1024
+constexpr int kOffReqPages = kOffMisc + 128;  // [kReqCache] int
+constexpr int kSmemBytes = kOffReqPages + kReqCache * 4 + 1024;  // + slack to align the base to 1024
 static_assert(kStages % kGroups == 0, "raw stage s is consumed by group s % kGroups only");
 static_assert(kStages <= 32, "one producer lane per raw stage");
+static_assert(kRecs % kRecChunk == 0 && kRecs - kRecChunk > kStages + kKTiles + 3 * kPipe,
+              "the record ring holds every page in flight");
 static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
 
 struct Misc {
@@ -144,31 +191,10 @@ struct Misc {
   int abort_flag;
   unsigned long long total;
   int b0, j0;
+  int stored[kPipe];  // last page issuer e has stored (-1 before the first)
 };
 
 __device__ __forceinline__ int pages_of(int seq, int cap) { return max(0, min(floor_div_page(seq - 1), cap)); }
-
-// Cursor over the (request, page) pairs in request order, skipping empty requests.
-struct Cursor {
-  const int32_t* seq_lens;
-  int B, cap, b, j, n;
-  __device__ void init(const int32_t* sl, int nb, int c, int b0, int j0) {
-    seq_lens = sl, B = nb, cap = c, b = b0, j = j0;
-    n = b < B ? pages_of(seq_lens[b], cap) : 0;
-  }
-  // Move k pages on; returns how many requests with pages were entered.
-  __device__ int advance(int k) {
-    j += k;
-    int entered = 0;
-    while (j >= n && b < B) {
-      j -= n;
-      ++b;
-      n = b < B ? pages_of(seq_lens[b], cap) : 0;
-      entered += n > 0;
-    }
-    return entered;
-  }
-};
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
@@ -223,6 +249,18 @@ __device__ __forceinline__ void write_query_tile(uint32_t taddr, const uint8_t* 
   tmem_wait_st();
 }
 
+// Shared-memory word accesses with release / acquire order (CTA scope).  The
+// store is issued only after `after` is computed (an input of the asm), so a
+// value derived from earlier loads' results orders it after those loads.
+__device__ __forceinline__ void st_release_shared_after(int* p, int v, uint32_t after) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v), "r"(after) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     const uint8_t* __restrict__ q, const float* __restrict__ q_scale, const uint8_t* __restrict__ kv,
     int64_t num_blocks, const int32_t* __restrict__ bt, int64_t bt_stride, int32_t max_blocks,
@@ -236,7 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   Misc* misc = reinterpret_cast<Misc*>(smem + kOffMisc);
   uint2* lut = reinterpret_cast<uint2*>(smem + kOffLut);
-  volatile int* valid_ring = reinterpret_cast<volatile int*>(smem + kOffValid);
+  PageRec* recs = reinterpret_cast<PageRec*>(smem + kOffRec);
+  float* score_slots = reinterpret_cast<float*>(smem + kOffScore);
+  int* req_pages = reinterpret_cast<int*>(smem + kOffReqPages);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cap = min(max_blocks, width);
@@ -246,15 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     misc->total = 0;
     misc->abort_flag = 0;
   }
+  if (tid < kPipe) misc->stored[tid] = -1;
   __syncthreads();
   {
     unsigned long long local = 0;
     bool clamped = false;
-    int* req_pages = reinterpret_cast<int*>(smem + kOffReqPages);
     for (int b = tid; b < num_reqs; b += kThreads) {
       const int seq = seq_lens[b];
       const int n = pages_of(seq, cap);
-      if (b < kThreads) req_pages[b] = n;  // the slice search below reads these from shared memory
+      if (b < kReqCache) req_pages[b] = n;  // the slice search and the page records read these
       local += (unsigned long long)n;
       clamped |= floor_div_page(seq - 1) > cap;
     }
@@ -263,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     if ((tid & 31) == 0 && local) atomicAdd(&misc->total, local);
   }
   __syncthreads();
+  // pages of request b (shared memory for the first kReqCache requests)
+  auto npages = [&](int b) -> int { return b < kReqCache ? req_pages[b] : pages_of(seq_lens[b], cap); };
   const unsigned long long P = misc->total;
   const unsigned long long p0 = P * blockIdx.x / gridDim.x, p1 = P * (blockIdx.x + 1) / gridDim.x;
   const int count = (int)(p1 - p0);
@@ -271,9 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     unsigned long long acc = 0;
     for (int base = 0; base < num_reqs; base += 32) {
       const int b = base + lane;
-      const int* req_pages = reinterpret_cast<const int*>(smem + kOffReqPages);
-      const unsigned long long n =
-          b >= num_reqs ? 0ull : (unsigned long long)(b < kThreads ? req_pages[b] : pages_of(seq_lens[b], cap));
+      const unsigned long long n = b >= num_reqs ? 0ull : (unsigned long long)npages(b);
       unsigned long long incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -305,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       mbar_init(&bars[kAccFull + s], 1);   // the MMA that wrote it
       mbar_init(&bars[kAccEmpty + s], 1);  // the epilogue that read it (and wrote the query tile)
       mbar_init(&bars[kDrain + s], 1);
+      mbar_init(&bars[kSlotDone + s], 1);  // the epilogue, once its last page's slot is filled
     }
     fence_mbar_init();
   }
@@ -322,48 +363,85 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
   const int b0 = misc->b0, j0 = misc->j0;
 
   if (warp == kProducerWarp) {
-    // ---------------- producer: raw pages into the ring ----------------
-    // Lane s < kStages owns ring stage s and fills it with pages i = s (mod
-    // kStages).  Each lane polls its own stage's empty barrier without
-    // blocking, so a stage is refilled as soon as its dequant group has
-    // loaded the page it held, whatever the other stages are doing: with a
-    // blocking wait per lane the warp moved on only when the slowest stage
-    // of a round of eight was free, and early stages stood empty for most of
-    // a round.  Block ids are loaded one page ahead.
+    // ---------------- producer: page records, raw pages into the ring ----------------
+    // Records: lane l writes page g + l's record.  Copies: lane s < kStages
+    // owns ring stage s and fills it with pages i = s (mod kStages) once
+    // their records exist.  Each lane polls its own stage's empty barrier
+    // without blocking, so a stage is refilled as soon as its dequant group
+    // has loaded the page it held, whatever the other stages are doing.
     const bool owner = lane < kStages;
-    Cursor lc;
-    lc.init(seq_lens, num_reqs, cap, b0, j0);
-    if (owner) lc.advance(lane);
-    int i = lane;  // the next page this lane copies
-    int64_t blk = (owner && i < count) ? (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j] : -1;
-    int64_t blk_next = -1;
-    if (owner && i + kStages < count) {
-      lc.advance(kStages);
-      blk_next = (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j];
-    }
-    int last = -1;      // the last page this lane copied into its stage
-    uint32_t idle = 0;  // polls in a row without progress in any lane
+    int gen = 0;              // pages with records
+    int gb = b0, gj = j0;     // (request, page) of page `gen`
+    int i = lane;             // the next page this lane copies
+    int last = -1;            // the last page this lane copied into its stage
+    uint32_t idle = 0;        // polls in a row without progress in any lane
     while (true) {
-      const bool active = owner && i < count;
-      if (!__any_sync(0xFFFFFFFFu, active)) break;
       bool progressed = false;
-      if (active && mbar_try_wait_nosuspend(&bars[kRawEmpty + lane], ((uint32_t)(i / kStages) & 1u) ^ 1u)) {
-        const bool valid = blk >= 0 && blk < num_blocks;
-        valid_ring[i % kRing] = valid ? 1 : 0;
-        if (valid) {
+      // records of pages below gen + 32 - kRecs are rewritten: every issuer
+      // must have stored all of its pages below that (its last stored page is
+      // then at least kPipe below it)
+      const int reuse = gen + kRecChunk - kRecs;
+      if (gen < count &&
+          (reuse <= 0 || min(min(ld_acquire_shared(&misc->stored[0]), ld_acquire_shared(&misc->stored[1])),
+                             ld_acquire_shared(&misc->stored[2])) >= reuse - kPipe)) {
+        // records of pages [gen, gen + 32): every lane walks from the chunk's
+        // first page to its own, and three pages on (the next page of the
+        // same accumulator), over the per-request page counts
+        int nb = npages(gb);
+        while (gj >= nb && gb < num_reqs) {
+          gj -= nb;
+          ++gb;
+          nb = gb < num_reqs ? npages(gb) : 0;
+        }
+        const int p = gen + lane;
+        int b = gb, j = gj + lane, n = nb;
+        while (j >= n && b < num_reqs) {
+          j -= n;
+          ++b;
+          n = b < num_reqs ? npages(b) : 0;
+        }
+        int b3 = b, j3 = j + kPipe, n3 = n;
+        while (j3 >= n3 && b3 < num_reqs) {
+          j3 -= n3;
+          ++b3;
+          n3 = b3 < num_reqs ? npages(b3) : 0;
+        }
+        const bool live = p < count;
+        const int blk = live ? bt[(int64_t)b * bt_stride + j] : -1;
+        const int nq = (live && p + kPipe < count && b3 != b) ? b3 : -1;
+        // whether each request of the chunk has a q_scale that is not >= 0
+        // (the epilogue then reduces with min too)
+        bool neg = false;
+        const int bfirst = __shfl_sync(0xFFFFFFFFu, b, 0);
+        const int blast = __reduce_max_sync(0xFFFFFFFFu, live ? b : bfirst);
+        for (int bb = bfirst; bb <= blast; ++bb) {
+          const bool any = __any_sync(0xFFFFFFFFu, !(q_scale[(int64_t)bb * kRows + lane] >= 0.f));
+          if (bb == b) neg = any;
+        }
+        if (nq >= 0) {
+          // the next request's query rows into L2 ahead of the epilogue's tile write
+          const uint8_t* qn = q + (int64_t)nq * kQBytes;
+          for (int k = 0; k < kQBytes; k += 128) prefetch_l2(qn + k);
+        }
+        if (live) recs[p % kRecs] = PageRec{b, j, blk, (nq + 1) | (neg ? kRecNeg : 0)};
+        gen = min(count, gen + kRecChunk);
+        gj += kRecChunk;
+        __syncwarp();  // every lane's records before any lane's copy
+        progressed = true;
+      }
+      const bool active = owner && i < count;
+      if (!__any_sync(0xFFFFFFFFu, active || gen < count)) break;
+      if (active && i < gen && mbar_try_wait_nosuspend(&bars[kRawEmpty + lane], ((uint32_t)(i / kStages) & 1u) ^ 1u)) {
+        const int blk = recs[i % kRecs].blk;
+        if (blk >= 0 && blk < num_blocks) {
           mbar_arrive_expect_tx(&bars[kRawFull + lane], kPageBytes);
-          bulk_g2s(smem + kOffRaw + lane * kPageBytes, kv + blk * kPageBytes, kPageBytes, &bars[kRawFull + lane]);
+          bulk_g2s(smem + kOffRaw + lane * kPageBytes, kv + (int64_t)blk * kPageBytes, kPageBytes,
+                   &bars[kRawFull + lane]);
         } else {
           mbar_arrive(&bars[kRawFull + lane]);
         }
         last = i;
         i += kStages;
-        blk = blk_next;
-        blk_next = -1;
-        if (i + kStages < count) {
-          lc.advance(kStages);
-          blk_next = (int64_t)bt[(int64_t)lc.b * bt_stride + lc.j];
-        }
         progressed = true;
       }
       if (__any_sync(0xFFFFFFFFu, progressed)) {
@@ -394,8 +472,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     // issue.
     const int e = issuer_of(warp);
     const uint32_t d = tmem + (uint32_t)e * kAccCols;
-    const uint32_t qa = tmem + kQCol0 + (uint32_t)e * kQCols;
-    bool issued_any = false;
+    const uint32_t qa = tmem + kQCol0 + (uint32_t)e * kQCols;  // A: all 128 lanes from lane 0
+    // scores of page p (released by the epilogue): lane = (slot, head) row
+    const int slot_q = lane >> 2, iq = slot_q - (kSlots - query_len);
+    int prev_b = -1, own = -1;
+    float qs = 0.f;
+    auto store_page = [&](int p) {
+      const PageRec r = recs[p % kRecs];
+      const float* sl = score_slots + score_slot(p) * 2 * kRows;
+      const float mx = sl[lane];
+      const float mn = (r.flags & kRecNeg) ? sl[kRows + lane] : 0.f;
+      // the record may be rewritten once every lane has read it: the ballot
+      // reads a value computed from every lane's loads
+      const uint32_t loaded = __ballot_sync(
+          0xFFFFFFFFu, (__float_as_uint(mx) ^ __float_as_uint(mn) ^ (uint32_t)(r.b ^ r.j ^ r.blk ^ r.flags)) == 0u);
+      if (lane == 0) st_release_shared_after(&misc->stored[e], p, loaded);
+      if (r.b != prev_b) {
+        prev_b = r.b;
+        qs = q_scale[(int64_t)prev_b * kRows + lane];
+        own = iq >= 0 ? floor_div_page(seq_lens[prev_b] - query_len + iq) : -1;
+      }
+      float val = qs >= 0.f ? qs * mx : qs * mn;
+      if (!(r.blk >= 0 && r.blk < num_blocks)) val = __int_as_float(0x7FC00000);  // NaN: ranked as -inf
+      if (r.j < own) scores[((int64_t)r.b * kRows + lane) * width + r.j] = val;
+    };
+    bool issued_any = false, ok = true;
+    int last = -1;  // the last page issued
     for (int i = e; i < count; i += kPipe) {
       const int tile = (i % kGroups) * kGroupTiles + (i / kGroups) % kGroupTiles;
       uint64_t* kt_full = &bars[kKtFull + tile * kPipe + e];
@@ -404,7 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       mbar_test2(kt_full, p_kt, &bars[kAccEmpty + e], p_acc, kt_ok, acc_ok);
       if (!kt_ok) kt_ok = timed_wait(kt_full, p_kt, misc, status, wait_polls);
       if (kt_ok && !acc_ok) acc_ok = timed_wait(&bars[kAccEmpty + e], p_acc, misc, status, wait_polls);
-      if (!__all_sync(0xFFFFFFFFu, kt_ok && acc_ok)) break;
+      if (!__all_sync(0xFFFFFFFFu, kt_ok && acc_ok)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       if (elect_one()) {
         const uint64_t bdesc = sw128_desc(sbase + kOffK + (uint32_t)tile * kKTile);
@@ -416,6 +521,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       }
       __syncwarp();
       issued_any = true;
+      last = i;
+      // the accumulator wait above was the epilogue's release of page i - 3,
+      // which came after it filled page i - 6's slot
+      if (i >= 2 * kPipe) store_page(i - 2 * kPipe);
+    }
+    if (issued_any && ok) {
+      // the last two pages, once the epilogue has filled the last page's slot
+      const bool rel = timed_wait(&bars[kSlotDone + e], 0u, misc, status, wait_polls);
+      if (__all_sync(0xFFFFFFFFu, rel)) {
+        if (last >= kPipe) store_page(last - kPipe);
+        store_page(last);
+      }
     }
     if (issued_any) {
       // all MMAs issued by this warp complete before TMEM is freed
@@ -427,41 +544,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     // ---------------- epilogue: lane = (slot, head) row ----------------
     const int e = epi_of(warp);  // pages i = e (mod 3), accumulator e
     const uint32_t quarter = (uint32_t)(32 * epi_quarter(e)) << 16;
-    Cursor cur;
-    cur.init(seq_lens, num_reqs, cap, b0, j0);
-    cur.advance(e);
-    const int slot = lane >> 2, iq = slot - (kSlots - query_len);
-    int prev_b = -1, own = -1;
-    float qs = 0.f;
-    bool neg = false;
     const uint32_t acc = tmem + quarter + (uint32_t)e * kAccCols;
     const uint32_t qa = tmem + quarter + kQCol0 + (uint32_t)e * kQCols;
     if (e < count) {
-      write_query_tile(qa, q + (int64_t)cur.b * kQBytes, lane);
+      // the request of this warp's first page: the slice start moved e pages on
+      int b = b0, j = j0 + e, n = npages(b);
+      while (j >= n && b < num_reqs) {
+        j -= n;
+        ++b;
+        n = b < num_reqs ? npages(b) : 0;
+      }
+      write_query_tile(qa, q + (int64_t)b * kQBytes, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kAccEmpty + e]);  // phase 0: query tile ready
     }
+    int last_i = -1;  // the last page handed to the issuer
     for (int i = e; i < count; i += kPipe) {
-      const int b = cur.b, j = cur.j;
-      cur.advance(kPipe);
-      // the issuer's next page (i + 3) belongs to another request: its query
-      // rows replace this tile once page i's MMA is complete
-      const bool next_q = i + kPipe < count && cur.b != b;
-      if (next_q) prefetch_l2(q + (int64_t)cur.b * kQBytes + lane * kHeadDim);
-      if (b != prev_b) {
-        prev_b = b;
-        qs = q_scale[(int64_t)b * kRows + lane];
-        neg = __any_sync(0xFFFFFFFFu, !(qs >= 0.f));
-        own = iq >= 0 ? floor_div_page(seq_lens[b] - query_len + iq) : -1;
-      }
       const bool ready = timed_wait(&bars[kAccFull + e], (uint32_t)(i / kPipe) & 1u, misc, status, wait_polls);
       if (!__all_sync(0xFFFFFFFFu, ready)) break;  // the TMEM loads below are warp-wide
       tc_fence_after();
-      const bool page_ok = valid_ring[i % kRing] != 0;
+      const int flags = recs[i % kRecs].flags;
       // three rounds of loads in flight (32 + 16, 32 + 16, 32 columns): the
       // register budget holds 48 loaded values at a time
-      float mx, mn = INFINITY;
+      float mx, mn = 0.f;
       {
         float r0, r1, r2, r3, r4;
         IDX_TMEM_LDRED32("max", acc, r0);
@@ -474,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
         tmem_wait_ld();
         mx = fmaxf(fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)), r4);
       }
-      if (neg) {
+      if (flags & kRecNeg) {
         float r0, r1, r2, r3, r4;
         IDX_TMEM_LDRED32("min", acc, r0);
         IDX_TMEM_LDRED16("min", acc + 32u, r1);
@@ -486,13 +592,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
         tmem_wait_ld();
         mn = fminf(fminf(fminf(r0, r1), fminf(r2, r3)), r4);
       }
-      if (next_q) write_query_tile(qa, q + (int64_t)cur.b * kQBytes, lane);
+      // the issuer's next page (i + 3) belongs to another request: its query
+      // rows replace this tile now that page i's MMA is complete
+      const int nq = (flags & kRecQueryMask) - 1;
+      if (nq >= 0) write_query_tile(qa, q + (int64_t)nq * kQBytes, lane);
       tc_fence_before();
-      __syncwarp();
+      __syncwarp();  // also orders the previous page's slot stores before the arrive
       if (lane == 0) mbar_arrive(&bars[kAccEmpty + e]);  // accumulator e (and its query tile) ready for page i + 3
-      float val = qs >= 0.f ? qs * mx : qs * mn;
-      if (!page_ok) val = __int_as_float(0x7FC00000);  // NaN: ranked as -inf
-      if (j < own) scores[((int64_t)b * kRows + lane) * width + j] = val;
+      // the row maxima (minima) into the page's score slot for the issuer
+      float* slot = score_slots + score_slot(i) * 2 * kRows;
+      slot[lane] = mx;
+      if (flags & kRecNeg) slot[kRows + lane] = mn;
+      last_i = i;
+    }
+    if (last_i >= 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kSlotDone + e]);  // the last page's slot is filled
     }
   } else if (is_dequant_warp(warp)) {
     // ---------------- dequant: 4 groups of 4 warps ----------------
@@ -519,7 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       }
       // codes and scales into registers, then the raw stage goes back to the
       // producer before the (longer) dequantisation
-      const bool page_valid = valid_ring[i % kRing] != 0;
+      const int blk = recs[i % kRecs].blk;
+      const bool page_valid = blk >= 0 && blk < num_blocks;
       uint4 cw[4];
       uint32_t sc[4];
       if (page_valid) {
