@@ -15,6 +15,9 @@ Modules:
 * ``indexer`` - NVFP4 page fields and dequantisation, decode page scores,
   64-bit page keys, exact top-16, decode row assembly, the decode step, and
   the multi-token relu-weighted scorer.
+* ``mxfp8`` - MXFP8 quantisation of bf16 rows (E8M0 block scales from the
+  amax's bit fields, E4M3 values), the epilogue that follows sparse decode
+  attention.
 
 Pins (checked by ``tests/test_oracle_*.py`` against the pages, closed forms
 and brute force, never against the CUDA path) are listed in each function's
