@@ -331,12 +331,11 @@ def run_native(args, wl, rank: int, world: int, dist):
     width, qlen = wl["width"], wl["query_len"]
     scores = torch.empty((B, 32, width), dtype=torch.float32, device="cuda")
     out = torch.empty((B, qlen, 4, 16), dtype=torch.int32, device="cuda")
-    ws_bytes = idx.idx_workspace_bytes(B * qlen * 4, width)
+    ws_bytes = idx.idx_decode_workspace_bytes(B, qlen, width)
     ws = torch.empty(max(8, ws_bytes) // 8, dtype=torch.int64, device="cuda") if ws_bytes else None
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     units = decode_units(wl)
-    split = ws_bytes > 0
-    launches_per_step = 2 + (1 if split else 0)
+    launches_per_step = 2 + (1 if ws_bytes > 0 else 0)  # scorer, selector (+ split-row merge)
 
     def step():
         idx.idx_decode_step(q, qs, kv, bt, sl, qlen, scores, out, ws, status)
@@ -509,7 +508,7 @@ def secondary(args, torch, idx, W, timer, hbm_peak) -> dict:
         q, qs, kv, bt, sl = (to_dev(wl[k]) for k in ("q", "q_scale", "kv", "bt", "seq_lens"))
         scores = torch.empty((16, 32, wl["width"]), dtype=torch.float32, device="cuda")
         out = torch.empty((16, 8, 4, 16), dtype=torch.int32, device="cuda")
-        wsb = idx.idx_workspace_bytes(16 * 32, wl["width"])
+        wsb = idx.idx_decode_workspace_bytes(16, 8, wl["width"])
         ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
         fn = lambda: idx.idx_decode_step(q, qs, kv, bt, sl, 8, scores, out, ws)
         fn()

@@ -92,11 +92,12 @@ int idx_have_qmul4(void);
 uint32_t idx_set_wait_limit(uint32_t polls);
 
 /*
- * Bytes of scratch workspace idx_topk16_select / idx_decode_step need for
- * `rows` rows of `width` columns (0 when rows fit one CTA each).  Rows longer
- * than 4,096 columns are split across CTAs whose local top-16s are merged
- * exactly through this workspace ([CP] module docstring: the global top 16
- * lies in the union of the partial top 16s).
+ * Bytes of scratch workspace idx_topk16_select needs for
+ * `rows` rows of `width` columns (0 when rows fit one CTA each: up to 8,192
+ * columns, 4,096 when there are few rows).  Longer rows are split across
+ * CTAs whose local top-16s are merged exactly through this workspace ([CP]
+ * module docstring: the global top 16 lies in the union of the partial top
+ * 16s).
  */
 size_t idx_workspace_bytes(int32_t rows, int32_t width);
 
@@ -206,12 +207,21 @@ int idx_topk16_select_noalloc(const float* scores, int64_t row_stride, int32_t r
  *   own + 1 <= 16 : pages 0..own, then -1;
  *   otherwise     : the 15 best pages below own among those scored, by
  *                   (score desc, page asc), then own.
+ * The rows are ranked by the top-16 selector over the score buffer (rows
+ * longer than 4,096 columns split across CTAs and merged exactly).
  *   scores_ws     [num_reqs, 32, width] float32 scratch the step scores into
  *                 (left holding the scores afterwards).
  *   out           [num_reqs, query_len, 4, 16] int32.
- *   workspace     >= idx_workspace_bytes(num_reqs * query_len * 4, width) bytes.
+ *   workspace     >= idx_decode_workspace_bytes(num_reqs, query_len, width)
+ *                 bytes, 8-byte aligned; its contents need no initialisation
+ *                 (NULL when that is 0).
  * Other arguments as in idx_score_pages.
+ *
+ * idx_decode_workspace_bytes: the selector's workspace for the step's
+ * num_reqs * query_len * 4 rows of `width` columns, i.e.
+ * idx_workspace_bytes(num_reqs * query_len * 4, width); 0 for a bad shape.
  */
+size_t idx_decode_workspace_bytes(int32_t num_reqs, int32_t query_len, int32_t width);
 int idx_decode_step(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
                     const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                     const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
@@ -240,6 +250,28 @@ int idx_mtp_score_fp8(const uint8_t* q, const float* q_scale, int32_t num_tokens
                       const uint8_t* k, const float* k_scale, int64_t num_blocks, const int32_t* block_table,
                       int64_t bt_stride, int32_t max_blocks, const int32_t* num_keys, const int32_t* cu_tokens,
                       int32_t num_reqs, int32_t max_keys, float* out, int32_t* status, void* stream);
+
+/*
+ * MXFP8 quantisation of bf16 rows ("vLLM PR #65508", the description of the
+ * epilogue that quantises the sparse-decode attention output for o_proj):
+ * per block of 32 consecutive elements of a row, with amax the largest
+ * magnitude (compared on the bf16 bit patterns, sign cleared),
+ *     scale = clamp(exponent_field(amax) - 8 + (mantissa(amax) > 0.75), 0, 254)
+ * (an E8M0 byte; = ceil(log2(amax / 448)) + 127), and every element becomes
+ *     e4m3_rn_satfinite(x * 2^(127 - scale)).
+ *
+ *   x_bf16        [rows, x_stride] bf16 bit patterns, 16-byte aligned,
+ *                 x_stride a multiple of 8; columns [0, cols) are read.
+ *   cols          a multiple of 32.
+ *   out_e4m3      [rows, out_stride] E4M3 bytes, 8-byte aligned, out_stride
+ *                 a multiple of 8.
+ *   scales_e8m0   [rows, scale_stride] bytes, row-major: scale of block k of
+ *                 row r at r * scale_stride + k.
+ * Finite inputs never saturate (the scaled block's largest magnitude is at
+ * most 448); an infinity becomes +-448, a NaN 0x7F.
+ */
+int idx_mxfp8_quantize(const uint16_t* x_bf16, int64_t rows, int64_t cols, int64_t x_stride, uint8_t* out_e4m3,
+                       int64_t out_stride, uint8_t* scales_e8m0, int64_t scale_stride, void* stream);
 
 #ifdef __cplusplus
 }

@@ -20,6 +20,7 @@ __all__ = [
     "idx_strerror",
     "idx_have_qmul4",
     "idx_workspace_bytes",
+    "idx_decode_workspace_bytes",
     "idx_set_wait_limit",
     "DEFAULT_WAIT_POLLS",
     "idx_dequant_nvfp4_pages",
@@ -29,6 +30,7 @@ __all__ = [
     "NOALLOC_SCRATCH_BYTES",
     "idx_decode_step",
     "idx_mtp_score_fp8",
+    "idx_mxfp8_quantize",
     "SYMBOLS",
     "ST_BLOCK_OOR",
     "ST_LEN_CLAMPED",
@@ -57,6 +59,7 @@ SYMBOLS = {
     "idx_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "idx_have_qmul4": (ctypes.c_int, []),
     "idx_workspace_bytes": (_sz, [_i32, _i32]),
+    "idx_decode_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "idx_set_wait_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
     "idx_dequant_nvfp4_pages": (ctypes.c_int, [_p, _i64, _p, _i64, _i32, _p, _p, _i32, _i32, _p, _i64, _p, _p]),
     "idx_score_pages": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p]),
@@ -64,6 +67,7 @@ SYMBOLS = {
     "idx_topk16_select_noalloc": (ctypes.c_int, [_p, _i64, _i32, _i32, _p, _i32, _i32, _p, _p, _p]),
     "idx_decode_step": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p, _sz, _p, _p]),
     "idx_mtp_score_fp8": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _p, _i64, _i32, _p, _p, _i32, _i32, _p, _p, _p]),
+    "idx_mxfp8_quantize": (ctypes.c_int, [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p]),
 }
 
 
@@ -146,6 +150,10 @@ def idx_workspace_bytes(rows: int, width: int) -> int:
     return int(load_library().idx_workspace_bytes(rows, width))
 
 
+def idx_decode_workspace_bytes(num_reqs: int, query_len: int, width: int) -> int:
+    return int(load_library().idx_decode_workspace_bytes(num_reqs, query_len, width))
+
+
 def idx_set_wait_limit(polls: int) -> int:
     """Set the tensor-core kernels' pipeline-wait budget (suspended polls); returns the previous one."""
     return int(load_library().idx_set_wait_limit(int(polls)))
@@ -213,3 +221,11 @@ def idx_mtp_score_fp8(q, q_scale, k, k_scale, block_table, num_keys, cu_tokens, 
         _ptr(q), _ptr(q_scale), q.shape[0], q.shape[1], _ptr(k), _ptr(k_scale), k.shape[0], _ptr(block_table),
         _row_stride(block_table), block_table.shape[1], _ptr(num_keys), _ptr(cu_tokens), num_keys.shape[0],
         int(max_keys), _ptr(out), _ptr(status), _stream(stream)))
+
+
+def idx_mxfp8_quantize(x, out, scales, stream=None) -> int:
+    """x [rows, cols] bf16 -> out [rows, cols] E4M3 bytes (uint8), scales [rows, cols // 32] E8M0 bytes (uint8)."""
+    lib = load_library()
+    return _check("idx_mxfp8_quantize", lib.idx_mxfp8_quantize(
+        _ptr(x), x.shape[0], x.shape[1], x.stride(0), _ptr(out), out.stride(0), _ptr(scales), scales.stride(0),
+        _stream(stream)))

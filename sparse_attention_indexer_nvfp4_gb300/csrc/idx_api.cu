@@ -11,12 +11,12 @@
 
 namespace idx {
 
-int launch_score_fma(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
-                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
-                     int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream);
 int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
                     int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream);
+int launch_score_fma(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
+                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
+                     int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream);
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -140,6 +140,11 @@ extern "C" int idx_score_pages(const uint8_t* q, const float* q_scale, const uin
                             query_len, width, scores, status, (cudaStream_t)stream);
 }
 
+extern "C" size_t idx_decode_workspace_bytes(int32_t num_reqs, int32_t query_len, int32_t width) {
+  if (num_reqs <= 0 || query_len < 1 || query_len > idx::kSlots) return 0;
+  return idx::topk_workspace_bytes(num_reqs * query_len * idx::kHeads, width);
+}
+
 extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
                                const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                                const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
@@ -157,8 +162,7 @@ extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uin
                           query_len, width, scores_ws);
     if (rc != IDX_OK) return rc;
   }
-  const int32_t rows = num_reqs * query_len * kHeads;
-  const size_t need = topk_workspace_bytes(rows, width);
+  const size_t need = idx_decode_workspace_bytes(num_reqs, query_len, width);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return IDX_E_WORKSPACE;
   if ((rc = check_device()) != IDX_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;

@@ -107,6 +107,8 @@ int launch_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv
                        int32_t num_reqs, int32_t query_len, int32_t width, float* scores, int32_t* status,
                        cudaStream_t stream);
 
+
+
 int launch_topk_plain(const float* scores, int64_t row_stride, int32_t rows, int32_t width, const int32_t* valid_n,
                       int32_t force_begin, int32_t force_end, int32_t* out_idx, uint64_t* out_keys, void* ws,
                       cudaStream_t stream);

@@ -1,0 +1,222 @@
+// Warp-level exact top-16 primitives over 64-bit page keys, shared by the
+// top-16 selector and the decode scorer's fused selection.
+//
+// Selection follows "wolfcomos/MSA PR #1" (section Changes): one warp ranks a
+// run of columns; every lane takes its largest key, every key at or above the
+// 16th largest of the 32 lane maxima survives (at least 16 do, about 20 for
+// random scores), survivors go to shared-memory slots and each is ranked by
+// counting the survivors above it, so the result does not depend on slot
+// order; with more than 64 survivors the warp falls back to 16 exact rounds.
+//
+// The first pass over a run of scores works on the 32-bit order-preserving
+// image of each score (the upper half of its key) and builds full keys only
+// for survivors: the threshold is the 16th largest lane maximum of those
+// images, so every key of the top 16 still survives (16 lane maxima lie at
+// or above it, each a distinct key at least as large), ties in the image
+// only add survivors.
+#pragma once
+
+#include "idx_common.cuh"
+
+namespace idx {
+namespace sel {
+
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr int kMergePerLane = 32;  // candidates per lane per merge pass
+constexpr int kMaxSurvivors = 64;
+constexpr uint32_t kOrderedPosInf = 0xFF800000u;  // image of +inf (forced columns)
+
+struct WarpScratch {
+  uint64_t surv[kMaxSurvivors];
+  uint64_t top[kTopK];
+};
+
+// Order-preserving 32-bit image of a score, the upper half of make_key:
+// NaN -> -inf (fmaxf returns the non-NaN operand), -0 -> +0 (adding +0),
+// then the sign-magnitude to unsigned order flip.  Every real score maps
+// to at least image(-inf) = 0x007FFFFF, so 0 is free to mean "no column".
+__device__ __forceinline__ uint32_t ordered_bits(float x) {
+  const float y = fmaxf(x, -INFINITY) + 0.0f;
+  const uint32_t b = __float_as_uint(y);
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t key_from(uint32_t image, int col) {
+  return ((uint64_t)image << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)col);
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(kFull, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+// Bitonic sort of one key per lane across the warp, descending (lane 0 largest).
+__device__ __forceinline__ uint64_t warp_sort_desc_u64(uint64_t v) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t w = __shfl_xor_sync(kFull, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      const uint64_t mx = w > v ? w : v, mn = w > v ? v : w;
+      v = keep_max ? mx : mn;
+    }
+  }
+  return v;
+}
+
+// Bitonic sort of one 32-bit value per lane across the warp, descending.
+__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint32_t w = __shfl_xor_sync(kFull, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_max ? max(v, w) : min(v, w);
+    }
+  }
+  return v;
+}
+
+// Rank `count` (<= 64) distinct survivor keys in ws->surv; lanes 0..15 of
+// the result hold the largest 16, descending, 0 padding.
+__device__ __forceinline__ uint64_t rank_survivors(uint32_t count, WarpScratch* ws) {
+  const uint32_t lane = lane_id();
+  const uint64_t a = lane < count ? ws->surv[lane] : 0;
+  const uint64_t b = lane + 32 < count ? ws->surv[lane + 32] : 0;
+  int ra = 0, rb = 0;
+  if (count <= 32) {
+    for (uint32_t j = 0; j < count; ++j) ra += ws->surv[j] > a;
+  } else {
+    for (uint32_t j = 0; j < count; ++j) {
+      const uint64_t v = ws->surv[j];
+      ra += v > a;
+      rb += v > b;
+    }
+  }
+  __syncwarp();
+  if (lane < count && ra < kTopK) ws->top[ra] = a;
+  if (lane + 32 < count && rb < kTopK) ws->top[rb] = b;
+  __syncwarp();
+  const uint64_t result = lane < min(count, (uint32_t)kTopK) ? ws->top[lane] : 0;
+  __syncwarp();
+  return result;
+}
+
+// New running top-16 of (running top-16) U (K keys per lane).  `run` holds the
+// running keys in lanes 0..15, descending, 0 padding; the result has the same
+// layout.  Keys are distinct except the 0 that marks "no candidate".
+template <int K>
+__device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, WarpScratch* ws) {
+  const uint32_t lane = lane_id();
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint64_t m = run;
+#pragma unroll
+  for (int i = 0; i < K; ++i) m = k[i] > m ? k[i] : m;
+  uint64_t thr = __shfl_sync(kFull, warp_sort_desc_u64(m), 15);
+  if (thr == 0) thr = 1;  // fewer than 16 candidates: every real key survives
+
+  uint32_t count = 0;
+  {
+    const bool p = run >= thr;
+    const uint32_t b = __ballot_sync(kFull, p);
+    const uint32_t pos = count + __popc(b & lt_mask);
+    if (p && pos < kMaxSurvivors) ws->surv[pos] = run;
+    count += __popc(b);
+  }
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    const bool p = k[i] >= thr;
+    const uint32_t b = __ballot_sync(kFull, p);
+    if (b) {
+      const uint32_t pos = count + __popc(b & lt_mask);
+      if (p && pos < kMaxSurvivors) ws->surv[pos] = k[i];
+      count += __popc(b);
+    }
+  }
+  __syncwarp();
+  if (count <= (uint32_t)kMaxSurvivors) return rank_survivors(count, ws);
+  // exact fallback: 16 rounds, each taking the largest key below the last
+  uint64_t result = 0, prev = ~0ull;
+  for (int r = 0; r < kTopK; ++r) {
+    uint64_t best = run < prev ? run : 0;
+#pragma unroll
+    for (int i = 0; i < K; ++i) best = (k[i] < prev && k[i] > best) ? k[i] : best;
+    best = warp_max_u64(best);
+    if ((int)lane == r) result = best;
+    prev = best;
+    if (best == 0) break;
+  }
+  __syncwarp();
+  return result;
+}
+
+// Top-16 keys of columns [c0, c1) of one fp32 row (c1 - c0 <= 32 * K): the
+// 32-bit image pass, keys built only for survivors.  Lanes 0..15 hold the
+// result, descending, 0 padding.
+// kCoherent loads through L2 (ld.global.cg) instead of the read-only path,
+// for scores written earlier in the same kernel.
+template <int K, bool kForce, bool kCoherent = false>
+__device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws) {
+  const uint32_t lane = lane_id();
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const int nch = (c1 - c0 + 31) >> 5;
+  uint32_t u[K];
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    const int col = c0 + i * 32 + (int)lane;
+    uint32_t v = 0;
+    if (i < nch && col < c1) {
+      v = ordered_bits(kCoherent ? __ldcg(row + col) : __ldg(row + col));
+      if (kForce && col >= fb && col < fe) v = kOrderedPosInf;
+    }
+    u[i] = v;
+  }
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < K; ++i) m = max(m, u[i]);
+  uint32_t thr = __shfl_sync(kFull, warp_sort_desc_u32(m), 15);
+  if (thr == 0) thr = 1;  // fewer than 16 columns: every one survives
+
+  uint32_t count = 0;
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    if (i < nch) {
+      const bool p = u[i] >= thr;
+      const uint32_t b = __ballot_sync(kFull, p);
+      if (b) {
+        const uint32_t pos = count + __popc(b & lt_mask);
+        if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(u[i], c0 + i * 32 + (int)lane);
+        count += __popc(b);
+      }
+    }
+  }
+  __syncwarp();
+  if (count <= (uint32_t)kMaxSurvivors) return rank_survivors(count, ws);
+  // exact fallback (many equal images): 16 rounds over the full keys
+  uint64_t result = 0, prev = ~0ull;
+  for (int r = 0; r < kTopK; ++r) {
+    uint64_t best = 0;
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      const uint64_t key = u[i] ? key_from(u[i], c0 + i * 32 + (int)lane) : 0ull;
+      best = (key < prev && key > best) ? key : best;
+    }
+    best = warp_max_u64(best);
+    if ((int)lane == r) result = best;
+    prev = best;
+    if (best == 0) break;
+  }
+  __syncwarp();
+  return result;
+}
+
+}  // namespace sel
+}  // namespace idx

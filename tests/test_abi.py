@@ -91,6 +91,15 @@ def test_one_row_stride_is_checked(built):
     assert lib.idx_topk16_select_noalloc(16, 10, 1, 100, None, 0, 0, 16, None, None) == -2
 
 
+def test_decode_workspace_sizing(built):
+    # the selector's workspace for the step's num_reqs * query_len * 4 rows
+    for b, ql, w in [(64, 8, 1344), (64, 1, 1344), (16, 8, 3906), (16, 1, 5000), (3, 5, 9000)]:
+        assert built.idx_decode_workspace_bytes(b, ql, w) == built.idx_workspace_bytes(b * ql * 4, w)
+    assert built.idx_decode_workspace_bytes(16, 8, 9000) > 0  # rows too long for one CTA split
+    assert built.idx_decode_workspace_bytes(0, 8, 1344) == 0
+    assert built.idx_decode_workspace_bytes(4, 9, 1344) == 0
+
+
 def test_workspace_sizing(built):
     # one CTA covers up to 4,096 columns; wider rows split across CTAs
     assert built.idx_workspace_bytes(100, 1) == 0

@@ -34,7 +34,7 @@ def _step(lib, wl, query_len=8):
     B = len(wl["seq_lens"])
     scores = sentinel_f32((B, 32, wl["width"]))
     out = torch.full((B, query_len, 4, 16), -9, dtype=torch.int32, device="cuda")
-    ws_bytes = lib.idx_workspace_bytes(B * query_len * 4, wl["width"])
+    ws_bytes = lib.idx_decode_workspace_bytes(B, query_len, wl["width"])
     ws = torch.empty(max(ws_bytes, 8) // 8, dtype=torch.int64, device="cuda") if ws_bytes else None
     st = status_word()
     lib.idx_decode_step(a["q"], a["q_scale"], a["kv"], a["block_table"], a["seq_lens"], query_len, scores, out, ws, st)
@@ -115,6 +115,17 @@ def test_clamped_lengths_and_bad_blocks(lib):
     s, out, st = _step(lib, wl)
     info, st_ref = _check_step(wl, s, out)
     assert st == st_ref and st & 1 and st & 2
+
+
+def test_fewer_pages_than_ctas(lib):
+    """About 80 pages over 120 scorer CTAs: a third of the CTAs get an empty
+    slice, some between a request's first and last CTA, so the fused
+    selection's merge must skip them."""
+    wl = W.decode_workload(39, 3, 3000, 4000, width=40, max_blocks=40)
+    s, out, st = _step(lib, wl)
+    info, st_ref = _check_step(wl, s, out)
+    assert st == st_ref == 0
+    assert info["near_tie_rows"] == 0
 
 
 def test_width_narrower_than_table(lib):

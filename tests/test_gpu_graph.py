@@ -28,7 +28,7 @@ def test_decode_step_graph_replay(lib):
     B, ql = len(wl["seq_lens"]), 8
     scores = sentinel_f32((B, 32, wl["width"]))
     out = torch.full((B, ql, 4, 16), -9, dtype=torch.int32, device="cuda")
-    wsb = lib.idx_workspace_bytes(B * ql * 4, wl["width"])
+    wsb = lib.idx_decode_workspace_bytes(B, ql, wl["width"])
     assert wsb > 0  # split rows: the merge kernel is captured too
     ws = torch.empty(wsb // 8, dtype=torch.int64, device="cuda")
     st = status_word()
