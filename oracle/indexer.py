@@ -273,16 +273,28 @@ def decode_row(own: int, scores_row: np.ndarray, n_scored: int) -> np.ndarray:
     return out.astype(np.int32)
 
 
-def decode_step(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, scores=None):
+def rank16(scores: np.ndarray) -> np.ndarray:
+    """Scores as the stock decode ranks them: rounded to 16 bits before ranking
+    ("vllm ... indexer_nvfp4_decode_cp", module docstring: the stock decode
+    ranks 16-bit quantized scores).  Reading: IEEE binary16, round to nearest
+    even, overflow to +-inf, NaN stays NaN; the result is widened back to
+    fp32 exactly, so keys are built as for any fp32 score and scores that tie
+    in 16 bits go to the lower page."""
+    return np.asarray(scores, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
+def decode_step(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, scores=None, rank_16bit=False):
     """Indexer decode step: out [B, query_len, 4, 16] int32.
 
     ``scores`` lets a test rank a given score buffer (for instance the GPU's
     own) instead of the oracle's, which checks the selection bit for bit.
+    ``rank_16bit`` ranks the scores after ``rank16``.
     Returns (out, scores, status).
     """
     status = 0
     if scores is None:
         scores, _, _, status = decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks)
+    ranked = rank16(scores) if rank_16bit else scores
     B = len(seq_lens)
     out = np.full((B, query_len, INDEX_HEADS, TOPK), -1, dtype=np.int32)
     for b in range(B):
@@ -291,7 +303,7 @@ def decode_step(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, scor
             slot = SLOTS - query_len + i
             own = own_page(seq_lens[b], query_len, i)
             for h in range(INDEX_HEADS):
-                out[b, i, h] = decode_row(own, scores[b, slot * INDEX_HEADS + h], n)
+                out[b, i, h] = decode_row(own, ranked[b, slot * INDEX_HEADS + h], n)
     return out, scores, status
 
 

@@ -151,3 +151,31 @@ def test_topk16_select_rows():
     idx, keys = topk16_select(data["scores"], data["valid_n"])
     for r in range(64):
         assert list(idx[r]) == brute_top16(data["scores"][r], int(data["valid_n"][r]))
+
+
+def test_rank16_rounds_to_binary16_by_hand():
+    """The 16-bit ranking's rounding, by hand from the binary16 format (10
+    fraction bits, largest finite 65504): exact values stay, ties go to the
+    even fraction, overflow past the last midpoint goes to infinity."""
+    from oracle.indexer import rank16
+
+    x = np.array([1.0 + 2.0 ** -10, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 65504.0, 65519.0, 65520.0, -65520.0,
+                  2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, np.nan], dtype=np.float32)
+    want = np.array([1.0 + 2.0 ** -10, 1.0, 1.0 + 2 * 2.0 ** -10, 65504.0, 65504.0, np.inf, -np.inf,
+                     2.0 ** -24, 0.0, 2.0 ** -24, np.nan], dtype=np.float32)
+    got = rank16(x)
+    assert np.array_equal(got[:-1], want[:-1]) and np.isnan(got[-1])
+
+
+def test_rank16_turns_near_ties_into_lower_page_ties():
+    """Two scores 2^-12 apart round to the same binary16 value, so the 16-bit
+    ranking puts the lower page first where fp32 ranking puts the larger."""
+    from oracle.indexer import decode_row, rank16
+
+    row = np.full(40, -5.0, dtype=np.float32)
+    row[3] = 1.0
+    row[30] = 1.0 + 2.0 ** -12
+    out32 = decode_row(35, row, 40)
+    out16 = decode_row(35, rank16(row), 40)
+    assert list(out32[:2]) == [30, 3] and list(out16[:2]) == [3, 30]
+    assert out32[15] == out16[15] == 35
