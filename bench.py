@@ -40,6 +40,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "indexer decode (query,head,page) scores/s + top-16 rows/s; index-K GB/s vs HBM peak"
+REPEATS = 5  # timed regions of K steps; the median is reported
 UNIT = "scores/s"
 PAGE_BYTES = 9216
 
@@ -225,6 +226,30 @@ class Timer:
         t.cuda.synchronize()
         return start.elapsed_time(end) / iters  # ms
 
+    def graph_median(self, fn, per_graph: int = 50, replays: int = 15) -> float:
+        """Median over `replays` replays of a CUDA graph of `per_graph` calls of
+        fn, in ms per call (for launches too short to time one by one)."""
+        t = self.torch
+        fn()
+        t.cuda.synchronize()
+        g = t.cuda.CUDAGraph()
+        with t.cuda.graph(g):
+            for _ in range(per_graph):
+                fn()
+        g.replay()
+        t.cuda.synchronize()
+        stream = t.cuda.current_stream()
+        vals = []
+        for _ in range(replays):
+            start = t.cuda.Event(enable_timing=True)
+            end = t.cuda.Event(enable_timing=True)
+            start.record(stream)
+            g.replay()
+            end.record(stream)
+            t.cuda.synchronize()
+            vals.append(start.elapsed_time(end) / per_graph)
+        return statistics.median(vals)
+
     def run_graph(self, fn, iters: int, per_graph: int = 20) -> float:
         """Like run(), for sequences of short kernels whose host-side launch
         cost would otherwise show up as idle gaps: `per_graph` calls of fn are
@@ -254,54 +279,55 @@ class Timer:
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
 
-def oracle_sample(wl, budget_s: float, seed: int = 0):
-    """Time the oracle on whole pages of the workload until ~budget_s seconds:
-    dequantise the page, score it for all 32 rows, rank a 1,344-column row.
-    Returns (scores per second, pages done, seconds)."""
-    from oracle.indexer import decode_scores, top16
+def cpu_baseline_samples(wl, seconds: float, repeats: int = 3):
+    """The oracle as it stands, timed on every host core: a pool of worker
+    processes (one per core of this process's affinity set) scores random
+    8-page runs of the workload's requests (dequantise each page, score it
+    for all 32 rows), `repeats` samples of about `seconds` each.  Returns
+    (median scores/s, cores, pages per sample, seconds per sample)."""
+    from oracle.pool import DecodeSampler
 
-    rng = np.random.default_rng(seed)
-    B = len(wl["seq_lens"])
-    t0 = time.perf_counter()
-    done_scores = pages = 0
-    rows_ranked = 0
-    while time.perf_counter() - t0 < budget_s:
-        b = int(rng.integers(0, B))
-        n = (int(wl["seq_lens"][b]) - 1) // 128
-        js = [int(j) for j in rng.integers(0, n, size=8)]
-        scores, written, _, _ = decode_scores(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"],
-                                              wl["query_len"], wl["width"], wl["max_blocks"],
-                                              pages=[(b, j) for j in js])
-        done_scores += int(written.sum())
-        pages += len(js)
-        row = np.nan_to_num(scores[b, 0], nan=-1.0)
-        top16(row, n)
-        rows_ranked += 1
-    dt = time.perf_counter() - t0
-    return done_scores / dt, pages, dt
+    sampler = DecodeSampler(wl, query_len=wl["query_len"])
+    try:
+        runs = [sampler.rate(seconds, seed=k) for k in range(repeats)]
+    finally:
+        sampler.close()
+    rates = sorted(r for r, _, _ in runs)
+    return rates[len(rates) // 2], sampler.cores, runs[0][1], statistics.median(dt for _, _, dt in runs)
 
 
 def run_reference(args, wl, rank: int):
+    """The reference arm: the CPU oracle (there is no other implementation
+    of this path to install), on all host cores, one bounded sample of the
+    workload per step; the rate is the median over the timed steps and
+    ms_per_step the time the oracle would take for one whole step at that
+    rate."""
     if rank != 0:
         return
-    budget = 4.0 if args.quick else 12.0
-    per_step = []
-    units = 0
-    for s in range(args.warmup + args.steps):
-        rate, pages, dt = oracle_sample(wl, budget / max(1, args.steps + args.warmup), seed=s)
-        if s >= args.warmup:
-            per_step.append((rate, pages, dt))
-    rate = sum(r * d for r, _, d in per_step) / sum(d for _, _, d in per_step)
-    pages = sum(p for _, p, _ in per_step)
-    ms = 1000.0 * sum(d for _, _, d in per_step) / len(per_step)
+    from oracle.pool import DecodeSampler
+
+    budget = 6.0 if args.quick else 20.0
+    per = max(0.5, budget / max(1, args.steps + args.warmup))
+    sampler = DecodeSampler(wl, query_len=wl["query_len"])
+    try:
+        runs = [sampler.rate(per, seed=s) for s in range(args.warmup + args.steps)][args.warmup:]
+    finally:
+        sampler.close()
+    rate = statistics.median(r for r, _, _ in runs)
+    units = decode_units(wl)
+    ms = 1000.0 * units["scores"] / rate
+    pages = sum(p for _, p, _ in runs)
+    sample = (f"{pages} random pages in 8-page runs over {len(runs)} timed samples of {per:.1f} s "
+              f"(dequant + 32-row scores each), {sampler.cores} worker processes")
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int64/f64 exact (oracle)", "data": "synthetic",
         "config": {"workload": "batched decode: 64 requests, seq_len U[8K,168K], 8 slots x 4 heads x 128, "
-                               "1,344-column rows, 1% duplicated pages", "seed": 2},
-        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{pages} random pages (dequant + 32-row scores + one top-16 row each)"},
+                               "1,344-column rows, 1% duplicated pages", "seed": 2,
+                   "timing": "ms_per_step = one whole step's scores at the median sampled rate; "
+                             f"each step samples {per:.1f} s"},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": sampler.cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -345,14 +371,22 @@ def run_native(args, wl, rank: int, world: int, dist):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
+    def timed(fn):
+        """REPEATS timed regions of exactly K steps, each bracketed by a
+        barrier and a synchronize; the median region's ms per step."""
+        vals = []
+        for _ in range(REPEATS):
+            if dist is not None:
+                dist.barrier()
+            torch.cuda.synchronize()
+            vals.append(timer.run(fn, args.steps))
+        return statistics.median(vals), vals
+
     sampler = ClockSampler(dev_idx)
     sampler.start()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ms = timer.run(step, args.steps)
+    ms, ms_repeats = timed(step)
     # dominant kernel: the decode scorer, timed alone over the same inputs
-    ms_score = timer.run(lambda: idx.idx_score_pages(q, qs, kv, bt, sl, qlen, scores, status), args.steps)
+    ms_score, _ = timed(lambda: idx.idx_score_pages(q, qs, kv, bt, sl, qlen, scores, status))
     clocks = sampler.stop()
 
     # End to end through the C ABI with host buffers: every step copies its
@@ -434,7 +468,7 @@ def run_native(args, wl, rank: int, world: int, dist):
 
     extra = {}
     if args.legs and rank == 0:
-        extra = secondary(args, torch, idx, W, timer, hbm_peak)
+        extra = secondary(args, torch, idx, W, timer, hbm_peak, dict(q=q, qs=qs, kv=kv, bt=bt, sl=sl, wl=wl))
 
     total_scores = units["scores"] * world
     value = whole_job_rate(units["scores"], world, ms)
@@ -451,6 +485,9 @@ def run_native(args, wl, rank: int, world: int, dist):
             "index_k_bytes_per_step": units["pages"] * PAGE_BYTES,
             "l2": "not flushed: the index-K pool (%.0f MB) exceeds the 129 MB L2" % (wl["kv"].nbytes / 1e6),
             "parallelism": f"replicas x{world}",
+            "timing": f"median of {REPEATS} timed regions of {args.steps} steps (CUDA events on the launching "
+                      "stream, barrier + synchronize around each)",
+            "ms_per_step_repeats": ms_repeats,
         },
         "rows_per_s": units["rows"] * world / (ms / 1000.0),
         "index_k_gbs": units["pages"] * PAGE_BYTES * world / (ms / 1000.0) / 1e9,
@@ -470,22 +507,83 @@ def run_native(args, wl, rank: int, world: int, dist):
         "extra": extra,
     }
     if rank == 0 and world == 1:
-        budget = 3.0 if args.quick else 12.0
-        rate, pages, dt = oracle_sample(wl, budget)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"{pages} random pages of the same workload in {dt:.1f} s "
-                                          "(dequant + 32-row scores each, plus a top-16 row per 8 pages)"}
+        seconds = 2.0 if args.quick else 5.0
+        rate, cores, pages, dt = cpu_baseline_samples(wl, seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"median of 3 samples of {dt:.1f} s, each ~{pages} random pages of the "
+                                          f"same workload in 8-page runs (dequant + 32-row scores), {cores} worker "
+                                          "processes (all cores of the affinity set)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def secondary(args, torch, idx, W, timer, hbm_peak) -> dict:
+def secondary(args, torch, idx, W, timer, hbm_peak, main) -> dict:
     """Other workloads of the path, each timed with CUDA events."""
     res = {}
     iters = max(3, args.steps // 4)
 
     def to_dev(x):
         return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    if "tiny" in args.legs:
+        # tiny decode: 1 request x 4,096 tokens, 31 pages scored
+        t = W.tiny_decode(0)
+        q, qs, kv, bt, sl = (to_dev(t[k]) for k in ("q", "q_scale", "kv", "bt", "seq_lens"))
+        sc = torch.empty((1, 32, t["width"]), dtype=torch.float32, device="cuda")
+        out = torch.empty((1, 8, 4, 16), dtype=torch.int32, device="cuda")
+        ms = timer.graph_median(lambda: idx.idx_decode_step(q, qs, kv, bt, sl, 8, sc, out), 50, 15)
+        u = decode_units(t)
+        res["tiny_decode"] = {"workload": "1 request x 4,096 tokens (31 pages scored), 8 slots x 4 heads",
+                              "us_per_step": ms * 1e3, "scores_per_s": u["scores"] / (ms / 1e3),
+                              "timing": "CUDA graph of 50 steps, median of 15 replays", "launches": 2}
+
+    if "qlen1" in args.legs:
+        # query_len 1 (4 live rows per request) on the batched workload: the
+        # CUDA-core scorer the library dispatches to, against the tensor-core
+        # scorer at query_len 2 (the same MMA work, 8 live rows)
+        m = main
+        sc = torch.empty((len(m["wl"]["seq_lens"]), 32, m["wl"]["width"]), dtype=torch.float32, device="cuda")
+        fma = timer.run(lambda: idx.idx_score_pages(m["q"], m["qs"], m["kv"], m["bt"], m["sl"], 1, sc), iters)
+        tc = timer.run(lambda: idx.idx_score_pages(m["q"], m["qs"], m["kv"], m["bt"], m["sl"], 2, sc), iters)
+        u1, u2 = decode_units(dict(m["wl"], query_len=1)), decode_units(dict(m["wl"], query_len=2))
+        res["query_len_1"] = {"workload": "batched decode, query_len 1 (4 live rows per request)",
+                              "ms_fma_scorer": fma, "ms_tensor_core_scorer_query_len_2": tc,
+                              "fma_index_k_gbs": u1["pages"] * PAGE_BYTES / (fma / 1e3) / 1e9,
+                              "tensor_core_index_k_gbs": u2["pages"] * PAGE_BYTES / (tc / 1e3) / 1e9,
+                              "dispatched": "fma" if fma < tc else "tensor core"}
+
+    if "sweep" in args.legs:
+        # standalone top-16: 4,096 rows per width, 1% specials and ties, ragged valid counts
+        out = torch.empty((4096, 16), dtype=torch.int32, device="cuda")
+        widths = {}
+        for w in W.SWEEP_WIDTHS:
+            d = W.topk_rows(100 + w, 4096, w)
+            x, vn = to_dev(d["scores"]), to_dev(d["valid_n"])
+            wsb = idx.idx_workspace_bytes(4096, w)
+            ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
+            ms = timer.graph_median(lambda: idx.idx_topk16_select(x, out, valid_n=vn, workspace=ws), 20, 15)
+            widths[str(w)] = {"us": ms * 1e3, "score_gbs": 4096 * w * 4 / (ms / 1e3) / 1e9,
+                              "rows_per_s": 4096 / (ms / 1e3)}
+            del x, vn, ws
+        res["topk_sweep"] = {"workload": "4,096 rows per width, 1% +-inf/NaN/+-0/FLT_MAX and ties, valid counts "
+                                         "0..width+8", "timing": "CUDA graph of 20 calls, median of 15 replays",
+                             "widths": widths}
+
+    if "mxfp8" in args.legs:
+        # MXFP8 quantisation of bf16 rows: a decode batch (16 rows x 2,048) and a large block (16,384 x 2,048)
+        rng = np.random.default_rng(5)
+        mx = {}
+        for rows in (16, 16384):
+            x = torch.from_numpy(rng.standard_normal((rows, 2048)).astype(np.float32)).cuda().to(torch.bfloat16)
+            o = torch.empty((rows, 2048), dtype=torch.uint8, device="cuda")
+            sc = torch.empty((rows, 64), dtype=torch.uint8, device="cuda")
+            ms = timer.graph_median(lambda: idx.idx_mxfp8_quantize(x, o, sc), 50 if rows == 16 else 10, 15)
+            byts = rows * 2048 * (2 + 1) + rows * 64
+            mx[str(rows)] = {"us": ms * 1e3, "gbs": byts / (ms / 1e3) / 1e9,
+                             "frac_of_hbm": byts / (ms / 1e3) / 1e9 / hbm_peak}
+        res["mxfp8"] = {"workload": "bf16 rows x 2,048 columns (32-element MX blocks)",
+                        "timing": "CUDA graph of 50 (16 rows) / 10 (16,384 rows) calls, median of 15 replays",
+                        "rows": mx}
 
     if "gather" in args.legs:
         # gather/dequant: 256 requests, num_pages U[1,1344], 200,000-page pool
@@ -559,8 +657,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip secondary workloads; short CPU baseline")
-    ap.add_argument("--legs", default="gather,long,mtp",
-                    help="secondary workloads to time (comma list of gather, long, mtp; empty for none)")
+    ap.add_argument("--legs", default="gather,long,mtp,tiny,qlen1,sweep,mxfp8",
+                    help="secondary workloads to time (comma list of gather, long, mtp, tiny, qlen1, sweep, mxfp8; "
+                         "empty for none)")
     args = ap.parse_args()
     args.legs = set() if args.quick else {x for x in args.legs.split(",") if x}
 

@@ -215,6 +215,12 @@ int idx_topk16_select_noalloc(const float* scores, int64_t row_stride, int32_t r
  *   workspace     >= idx_decode_workspace_bytes(num_reqs, query_len, width)
  *                 bytes, 8-byte aligned; its contents need no initialisation
  *                 (NULL when that is 0).
+ *   flags         0, or IDX_RANK_16BIT: rank the scores rounded to IEEE
+ *                 binary16 (round to nearest even, overflow to infinity),
+ *                 as the stock decode ranks 16-bit quantized scores ([CP]
+ *                 module docstring); scores equal in 16 bits then rank by
+ *                 page (lower first).  The score buffer keeps the fp32
+ *                 scores.  Other bits: IDX_E_BAD_SHAPE.
  * Other arguments as in idx_score_pages.
  *
  * idx_decode_workspace_bytes: the selector's workspace for the step's
@@ -222,11 +228,12 @@ int idx_topk16_select_noalloc(const float* scores, int64_t row_stride, int32_t r
  * idx_workspace_bytes(num_reqs * query_len * 4, width); 0 for a bad shape.
  */
 size_t idx_decode_workspace_bytes(int32_t num_reqs, int32_t query_len, int32_t width);
+#define IDX_RANK_16BIT 1
 int idx_decode_step(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
                     const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                     const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
                     float* scores_ws, int32_t* out, void* workspace, size_t workspace_bytes,
-                    int32_t* status, void* stream);
+                    int32_t flags, int32_t* status, void* stream);
 
 /*
  * Multi-token FP8 indexer scores [MTP]:

@@ -181,3 +181,61 @@ def mtp_scores_full(m: dict):
     for t, s, bd in parts:
         out[t], bound[t] = s, bd
     return out, bound
+
+
+# ---------------------------------------------------------------------------
+# timed samples (the CPU baseline of the benchmark)
+# ---------------------------------------------------------------------------
+
+def _decode_piece_count(task):
+    b, j0, j1, _, wr, _, _ = _decode_piece(task)
+    return int(wr.sum()), j1 - j0
+
+
+class DecodeSampler:
+    """A pool of workers holding one decode workload, timing the oracle on
+    random pieces of it (each piece: one request's run of `piece` pages,
+    dequantised and scored for all 32 rows)."""
+
+    def __init__(self, wl: dict, query_len: int = 8, piece: int = 8, processes: int | None = None):
+        from oracle.indexer import scored_pages
+
+        self.piece = piece
+        self.cores = processes or cores()
+        self.n = [scored_pages(s, wl["max_blocks"], wl["width"]) for s in wl["seq_lens"]]
+        self.shared = Shared({"kv": wl["kv"]})
+        small = {k: wl[k] for k in ("q", "q_scale", "bt", "seq_lens")}
+        small.update(query_len=query_len, width=int(wl["width"]), max_blocks=int(wl["max_blocks"]))
+        self.pool = mp.get_context("spawn").Pool(processes=self.cores, initializer=_init,
+                                                 initargs=(self.shared.spec, small))
+        first = next(b for b, n in enumerate(self.n) if n > 0)
+        self.pool.map(_decode_piece_count, [(first, 0, 1)] * self.cores)  # workers up and warm
+
+    def rate(self, seconds: float, seed: int = 0):
+        """Scores per second over about `seconds` with every worker busy,
+        pieces handed out in rounds of a few per worker; returns (rate, pages,
+        wall seconds)."""
+        import time
+
+        rng = np.random.default_rng(seed)
+        live = [b for b, n in enumerate(self.n) if n > 0]
+        done = pages = 0
+        t0 = time.perf_counter()
+        while True:
+            tasks = []
+            for _ in range(4 * self.cores):
+                b = int(rng.choice(live))
+                j0 = int(rng.integers(0, max(1, self.n[b] - self.piece + 1)))
+                tasks.append((b, j0, min(self.n[b], j0 + self.piece)))
+            for written, np_ in self.pool.map(_decode_piece_count, tasks, chunksize=1):
+                done += written
+                pages += np_
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+        return done / dt, pages, dt
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+        self.shared.close()

@@ -29,6 +29,7 @@ __all__ = [
     "idx_topk16_select_noalloc",
     "NOALLOC_SCRATCH_BYTES",
     "idx_decode_step",
+    "RANK_16BIT",
     "idx_mtp_score_fp8",
     "idx_mxfp8_quantize",
     "SYMBOLS",
@@ -65,7 +66,8 @@ SYMBOLS = {
     "idx_score_pages": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p]),
     "idx_topk16_select": (ctypes.c_int, [_p, _i64, _i32, _i32, _p, _i32, _i32, _p, _p, _p, _sz, _p]),
     "idx_topk16_select_noalloc": (ctypes.c_int, [_p, _i64, _i32, _i32, _p, _i32, _i32, _p, _p, _p]),
-    "idx_decode_step": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p, _sz, _p, _p]),
+    "idx_decode_step": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p, _sz, _i32, _p,
+                                       _p]),
     "idx_mtp_score_fp8": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _p, _i64, _i32, _p, _p, _i32, _i32, _p, _p, _p]),
     "idx_mxfp8_quantize": (ctypes.c_int, [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p]),
 }
@@ -202,15 +204,18 @@ def idx_topk16_select_noalloc(scores, out_idx, valid_n=None, force_begin: int = 
         _ptr(out_idx), _ptr(out_keys), _stream(stream)))
 
 
+RANK_16BIT = 1  # idx_decode_step flag: rank the scores rounded to binary16
+
+
 def idx_decode_step(q, q_scale, kv, block_table, seq_lens, query_len: int, scores_ws, out, workspace=None,
-                    status=None, stream=None) -> int:
+                    status=None, stream=None, flags: int = 0) -> int:
     """One decode step: scores into scores_ws [B,32,width], rows into out [B,query_len,4,16] i32."""
     lib = load_library()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return _check("idx_decode_step", lib.idx_decode_step(
         _ptr(q), _ptr(q_scale), _ptr(kv), kv.shape[0], _ptr(block_table), _row_stride(block_table),
         block_table.shape[1], _ptr(seq_lens), seq_lens.shape[0], int(query_len), scores_ws.shape[-1],
-        _ptr(scores_ws), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
+        _ptr(scores_ws), _ptr(out), _ptr(workspace), ws_bytes, int(flags), _ptr(status), _stream(stream)))
 
 
 def idx_mtp_score_fp8(q, q_scale, k, k_scale, block_table, num_keys, cu_tokens, max_keys: int, out, status=None,

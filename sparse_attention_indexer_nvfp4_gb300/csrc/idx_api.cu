@@ -149,9 +149,10 @@ extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uin
                                const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                                const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
                                float* scores_ws, int32_t* out, void* workspace, size_t workspace_bytes,
-                               int32_t* status, void* stream) {
+                               int32_t flags, int32_t* status, void* stream) {
   using namespace idx;
   if (num_reqs < 0 || width < 0 || max_blocks < 0 || query_len < 1 || query_len > kSlots) return IDX_E_BAD_SHAPE;
+  if ((flags & ~IDX_RANK_16BIT) != 0) return IDX_E_BAD_SHAPE;
   if (num_reqs == 0) return IDX_OK;
   if (!out || !seq_lens) return IDX_E_NULL_PTR;
   if (!aligned(out, 4) || !aligned(workspace, 8)) return IDX_E_MISALIGNED;
@@ -171,6 +172,7 @@ extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uin
                             query_len, width, scores_ws, status, s);
     if (rc != IDX_OK) return rc;
   }
-  DecodeRows d{scores_ws, seq_lens, num_reqs, query_len, width, any_pages ? max_blocks : 0, out};
+  DecodeRows d{scores_ws, seq_lens, num_reqs, query_len, width, any_pages ? max_blocks : 0, out,
+               (flags & IDX_RANK_16BIT) != 0};
   return launch_topk_decode(d, workspace, s);
 }

@@ -100,6 +100,7 @@ struct DecodeRows {
   const int32_t* seq_lens;
   int32_t num_reqs, query_len, width, max_blocks;
   int32_t* out;  // [B, query_len, 4, 16]
+  bool rank16;   // rank the scores rounded to binary16 (IDX_RANK_16BIT)
 };
 
 int launch_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,

@@ -161,10 +161,12 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
 // Top-16 keys of columns [c0, c1) of one fp32 row (c1 - c0 <= 32 * K): the
 // 32-bit image pass, keys built only for survivors.  Lanes 0..15 hold the
 // result, descending, 0 padding.
-// kCoherent loads through L2 (ld.global.cg) instead of the read-only path,
-// for scores written earlier in the same kernel.
-template <int K, bool kForce, bool kCoherent = false>
-__device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws) {
+// With rank16 every score is first rounded to binary16 (round to nearest
+// even, overflow to infinity) and widened back, so scores that tie in 16
+// bits rank by column.
+template <int K, bool kForce>
+__device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
+                                   bool rank16 = false) {
   const uint32_t lane = lane_id();
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int nch = (c1 - c0 + 31) >> 5;
@@ -174,7 +176,9 @@ __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1
     const int col = c0 + i * 32 + (int)lane;
     uint32_t v = 0;
     if (i < nch && col < c1) {
-      v = ordered_bits(kCoherent ? __ldcg(row + col) : __ldg(row + col));
+      float x = __ldg(row + col);
+      if (rank16) x = __half2float(__float2half_rn(x));
+      v = ordered_bits(x);
       if (kForce && col >= fb && col < fe) v = kOrderedPosInf;
     }
     u[i] = v;

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(128) k_topk_rows(PlainRows p, DecodeRows d, in
   const int c0 = kWarps == 1 ? 0 : (split * kWarps + (int)warp) * kSeg;
   const int c1 = min(c0 + kSeg, n);
   uint64_t run = 0;
-  if (c0 < c1) run = warp_top16_seg<K, !kDecode>(row, c0, c1, fb, fe, &scratch[warp]);
+  if (c0 < c1) run = warp_top16_seg<K, !kDecode>(row, c0, c1, fb, fe, &scratch[warp], kDecode && d.rank16);
   run = cta_merge<kWarps>(run, cand, &scratch[0]);
   if (kWarps > 1 && warp != 0) return;
   if (nsplit == 1) {

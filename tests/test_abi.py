@@ -64,7 +64,8 @@ def test_error_codes_and_strings(built):
     assert lib.idx_topk16_select(16, 100, 3, 100, None, 0, 0, 16, 12, None, 0, None) == E_MIS  # keys 8-aligned
     assert lib.idx_topk16_select(16, 100, 0, 100, None, 0, 0, None, None, None, 0, None) == 0
     assert lib.idx_mtp_score_fp8(16, 16, 4, 0, 16, 16, 8, 16, 4, 4, 16, 16, 2, 10, 16, None, None) == E_SHAPE
-    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 5000, 16, 16, None, 0, None, None) == E_WS
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 9000, 16, 16, None, 0, 0, None, None) == E_WS
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 2, None, None) == E_SHAPE  # flags
 
 
 def test_wait_limit_setter_returns_the_previous_budget(built):

@@ -29,7 +29,7 @@ def _scores(lib, wl, query_len=8):
     return host(scores), int(st.item())
 
 
-def _step(lib, wl, query_len=8):
+def _step(lib, wl, query_len=8, flags=0):
     a = decode_args(wl)
     B = len(wl["seq_lens"])
     scores = sentinel_f32((B, 32, wl["width"]))
@@ -37,7 +37,8 @@ def _step(lib, wl, query_len=8):
     ws_bytes = lib.idx_decode_workspace_bytes(B, query_len, wl["width"])
     ws = torch.empty(max(ws_bytes, 8) // 8, dtype=torch.int64, device="cuda") if ws_bytes else None
     st = status_word()
-    lib.idx_decode_step(a["q"], a["q_scale"], a["kv"], a["block_table"], a["seq_lens"], query_len, scores, out, ws, st)
+    lib.idx_decode_step(a["q"], a["q_scale"], a["kv"], a["block_table"], a["seq_lens"], query_len, scores, out, ws, st,
+                        flags=flags)
     torch.cuda.synchronize()
     return host(scores), host(out), int(st.item())
 
@@ -117,6 +118,30 @@ def test_clamped_lengths_and_bad_blocks(lib):
     assert st == st_ref and st & 1 and st & 2
 
 
+@pytest.mark.parametrize("scale", [1.0, 600.0])
+def test_rank_16bit_mode(lib, scale):
+    """The 16-bit ranking mode: rows bit-exact against the oracle's binary16
+    ranking of the GPU's own scores.  At q_scale x 600 many scores pass the
+    binary16 range and tie at +-infinity, so rows change from the fp32
+    ranking; the scores themselves stay fp32."""
+    wl = W.decode_workload(48, 6, 3000, 30000, width=240, max_blocks=240, dup_frac=0.02)
+    wl["q_scale"] = (wl["q_scale"] * scale).astype(np.float32)
+    s, out, st = _step(lib, wl, flags=lib.RANK_16BIT)
+    assert st == 0
+    sel16, _, _ = decode_step(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"], 8, wl["width"],
+                              wl["max_blocks"], scores=s, rank_16bit=True)
+    assert np.array_equal(out, sel16)
+    sel32, _, _ = decode_step(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"], 8, wl["width"],
+                              wl["max_blocks"], scores=s)
+    differ = int((sel16 != sel32).any(axis=-1).sum())
+    print(f"\n16-bit ranking, q_scale x {scale}: {differ} of {out.shape[0] * 8 * 4} rows differ from fp32 ranking")
+    if scale > 1.0:
+        assert differ > 0
+    ref, written, bound, _ = decode_scores(wl["q"], wl["q_scale"], wl["kv"], wl["bt"], wl["seq_lens"], 8,
+                                           wl["width"], wl["max_blocks"])
+    check_scores(s, ref, written, bound)  # the score buffer keeps fp32
+
+
 def test_fewer_pages_than_ctas(lib):
     """About 80 pages over 120 scorer CTAs: a third of the CTAs get an empty
     slice, some between a request's first and last CTA, so the fused
@@ -175,7 +200,7 @@ def _check_full(wl, s, out):
     host cores), the untouched pattern, the selection bit for bit on the
     GPU's own scores, and the end-to-end rows against the oracle's: the
     number of rows that differ at a near-tie is returned (expected 0)."""
-    import oracle_pool
+    from oracle import pool as oracle_pool
 
     ref, written, bound, st_ref = oracle_pool.decode_scores_full(wl, 8)
     info = check_scores(s, ref, written, bound)

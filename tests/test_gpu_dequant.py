@@ -90,7 +90,7 @@ def test_full_size_gather(lib):
     """256 requests, num_pages U[1,1344], 200,000-page pool, 2% special scales:
     every output byte is written (two sentinels give identical outputs) and
     every gathered page equals the oracle's byte for byte."""
-    import oracle_pool
+    from oracle import pool as oracle_pool
 
     wl = W.gather_workload(seed=1)
     args = (dev(wl["kv"]), dev(wl["bt"]), dev(wl["num_pages"]), dev(wl["page_offsets"]), wl["max_num_pages"])

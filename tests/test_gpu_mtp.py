@@ -65,7 +65,7 @@ def test_full_size(lib):
     """32 requests x 2 tokens x 64 heads, 32,768 keys per request: every token's
     scores against the oracle, the top-16 bit for bit on the GPU's scores, and
     no top-16 row differing from the oracle's (near-ties: 0)."""
-    import oracle_pool
+    from oracle import pool as oracle_pool
 
     wl = W.mtp_workload(seed=3)
     out, st = _run(lib, wl)

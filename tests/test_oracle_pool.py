@@ -3,7 +3,7 @@ call of the oracle on the whole workload returns (CPU only)."""
 
 import numpy as np
 
-import oracle_pool as P
+from oracle import pool as P
 from oracle.indexer import decode_scores, gather_dequant, mtp_scores
 from sparse_attention_indexer_nvfp4_gb300 import workloads as W
 
