@@ -539,18 +539,17 @@ def secondary(args, torch, idx, W, timer, hbm_peak, main) -> dict:
 
     if "qlen1" in args.legs:
         # query_len 1 (4 live rows per request) on the batched workload: the
-        # CUDA-core scorer the library dispatches to, against the tensor-core
-        # scorer at query_len 2 (the same MMA work, 8 live rows)
+        # decode step and its scorer (the tensor-core kernel at every query_len)
         m = main
-        sc = torch.empty((len(m["wl"]["seq_lens"]), 32, m["wl"]["width"]), dtype=torch.float32, device="cuda")
-        fma = timer.run(lambda: idx.idx_score_pages(m["q"], m["qs"], m["kv"], m["bt"], m["sl"], 1, sc), iters)
-        tc = timer.run(lambda: idx.idx_score_pages(m["q"], m["qs"], m["kv"], m["bt"], m["sl"], 2, sc), iters)
-        u1, u2 = decode_units(dict(m["wl"], query_len=1)), decode_units(dict(m["wl"], query_len=2))
+        B = len(m["wl"]["seq_lens"])
+        sc = torch.empty((B, 32, m["wl"]["width"]), dtype=torch.float32, device="cuda")
+        out1 = torch.empty((B, 1, 4, 16), dtype=torch.int32, device="cuda")
+        score = timer.run(lambda: idx.idx_score_pages(m["q"], m["qs"], m["kv"], m["bt"], m["sl"], 1, sc), iters)
+        step1 = timer.run(lambda: idx.idx_decode_step(m["q"], m["qs"], m["kv"], m["bt"], m["sl"], 1, sc, out1), iters)
+        u1 = decode_units(dict(m["wl"], query_len=1))
         res["query_len_1"] = {"workload": "batched decode, query_len 1 (4 live rows per request)",
-                              "ms_fma_scorer": fma, "ms_tensor_core_scorer_query_len_2": tc,
-                              "fma_index_k_gbs": u1["pages"] * PAGE_BYTES / (fma / 1e3) / 1e9,
-                              "tensor_core_index_k_gbs": u2["pages"] * PAGE_BYTES / (tc / 1e3) / 1e9,
-                              "dispatched": "fma" if fma < tc else "tensor core"}
+                              "ms_step": step1, "ms_scorer": score, "scores_per_s": u1["scores"] / (step1 / 1e3),
+                              "index_k_gbs": u1["pages"] * PAGE_BYTES / (score / 1e3) / 1e9}
 
     if "sweep" in args.legs:
         # standalone top-16: 4,096 rows per width, 1% specials and ties, ragged valid counts
