@@ -371,3 +371,74 @@ def mtp_scores(q, q_scale, k, k_scale, bt, num_keys, cu_tokens, max_keys, tokens
             out[t, :nk] = np.where(valid, s, np.float32(np.nan))
             bound[t, :nk] = np.where(valid, b, 0.0)
     return out, bound
+
+
+# ---------------------------------------------------------------------------
+# prefill (Q8KV8) chain
+# ---------------------------------------------------------------------------
+
+def prefill_positions(num_keys, cu_tokens) -> np.ndarray:
+    """Position of every prefill token: request r's n_r new tokens are the
+    last n_r of its num_keys[r] keys, token i (of n_r) at num_keys[r] - n_r + i
+    (the reading the decode path uses for its own page)."""
+    T = int(cu_tokens[-1])
+    pos = np.zeros(T, dtype=np.int64)
+    for r in range(len(num_keys)):
+        t0, t1 = int(cu_tokens[r]), int(cu_tokens[r + 1])
+        for t in range(t0, t1):
+            pos[t] = int(num_keys[r]) - (t1 - t0) + (t - t0)
+    return pos
+
+
+def prefill_step(kv, bt, num_keys, cu_tokens, q, q_scale, max_keys):
+    """The Q8KV8 prefill indexer chain, stated plainly.
+
+    * Gather and dequantise each request's NVFP4 index-K pages to E4M3
+      ("vllm ... ops.gather_nvfp4_index_k": the pages feed the Q8KV8 prefill
+      indexer), ceil(num_keys / 128) pages of request r.
+    * Score every token against its request's keys with the relu-weighted head
+      sum of "Mojo module sparse_index_fp8_sm100" (k_scale 1: the block scales
+      are inside the dequantised values).
+    * Causal mask and -inf tail fill (the same page's "prefill / causal
+      masking and the -inf tail-fill fusion"): keys past the token's position
+      and every column from num_keys to max_keys score -inf.
+    * Top-16 per token over its visible keys [0, min(position + 1, num_keys,
+      max_keys)), key order as everywhere ("wolfcomos/MSA PR #1": the prefill
+      top-k promises cutoff ties to the lower id, matching the merge), -1 pad.
+
+    Returns (scores [T, max_keys] f32, bound [T, max_keys] f64, visible [T],
+    out [T, 16] int32, status).
+    """
+    kv = np.asarray(kv).reshape(-1, PAGE_BYTES)
+    T = int(cu_tokens[-1])
+    scores = np.full((T, max_keys), -np.inf, dtype=np.float32)
+    bound = np.zeros((T, max_keys), dtype=np.float64)
+    pos = prefill_positions(num_keys, cu_tokens)
+    visible = np.zeros(T, dtype=np.int64)
+    status = 0
+    for r in range(len(num_keys)):
+        nk = max(0, min(int(num_keys[r]), int(max_keys), bt.shape[1] * PAGE_TOKENS))
+        npg = -(-nk // PAGE_TOKENS)
+        keys = np.zeros((npg * PAGE_TOKENS, HEAD_DIM), dtype=np.uint8)
+        valid = np.ones(npg * PAGE_TOKENS, dtype=bool)
+        for p in range(npg):
+            blk = int(bt[r, p])
+            if 0 <= blk < kv.shape[0]:
+                keys[p * PAGE_TOKENS:(p + 1) * PAGE_TOKENS] = dequant_page(kv[blk])
+            else:
+                status |= ST_BLOCK_OOR
+                valid[p * PAGE_TOKENS:(p + 1) * PAGE_TOKENS] = False
+        for t in range(int(cu_tokens[r]), int(cu_tokens[r + 1])):
+            visible[t] = max(0, min(int(pos[t]) + 1, nk))
+            if nk == 0:
+                continue
+            s, b = mtp_token_scores(q[t], q_scale[t], keys[:nk], np.ones(nk, dtype=np.float32))
+            cols = np.arange(nk)
+            keep = cols <= pos[t]
+            s = np.where(valid[:nk], s, np.float32(np.nan))
+            scores[t, :nk] = np.where(keep, s, np.float32(-np.inf))
+            bound[t, :nk] = np.where(keep & valid[:nk], b, 0.0)
+    out = np.full((T, TOPK), -1, dtype=np.int32)
+    for t in range(T):
+        out[t], _ = top16(scores[t], int(visible[t]))
+    return scores, bound, visible, out, status
