@@ -646,6 +646,27 @@ def secondary(args, torch, idx, W, timer, hbm_peak, main) -> dict:
                       "scorer_tflops": flops / (ms_s / 1e3) / 1e12, "scorer_gbs": kbytes / (ms_s / 1e3) / 1e9,
                       "scorer_frac_of_hbm": kbytes / (ms_s / 1e3) / 1e9 / hbm_peak, "launches": 2 + (1 if wsb else 0)}
 
+    if "prefill" in args.legs:
+        # Q8KV8 prefill chain: gather-dequant, causal relu-weighted scores, top-16 per token
+        pw = W.prefill_workload()
+        kv, bt, nk, cu, q, qs = (to_dev(pw[k]) for k in ("kv", "bt", "num_keys", "cu_tokens", "q", "q_scale"))
+        T, mk = int(pw["cu_tokens"][-1]), pw["max_keys"]
+        sc = torch.empty((T, mk), dtype=torch.float32, device="cuda")
+        out = torch.empty((T, 16), dtype=torch.int32, device="cuda")
+        ws = torch.empty(idx.idx_prefill_workspace_bytes(len(pw["num_keys"]), pw["bt"].shape[1], T, mk),
+                         dtype=torch.uint8, device="cuda")
+        fn = lambda: idx.idx_prefill_index_step(kv, bt, nk, cu, q, qs, mk, sc, out, ws)
+        fn()
+        ms = timer.run(fn, iters)
+        tok_keys = sum(int(pw["cu_tokens"][r + 1] - pw["cu_tokens"][r]) * int(n) for r, n in enumerate(pw["num_keys"]))
+        flops = 2.0 * pw["heads"] * 128 * tok_keys
+        res["prefill"] = {"workload": "chunked prefill: 4 requests x 16,384 keys, 2,048 new tokens each, 64 heads; "
+                                      "top-16 per token", "ms": ms, "token_keys_per_s": tok_keys / (ms / 1e3),
+                          "tflops": flops / (ms / 1e3) / 1e12, "launches": 4 + (1 if idx.idx_workspace_bytes(T, mk)
+                                                                                 else 0)}
+        del kv, bt, nk, cu, q, qs, sc, out, ws
+        torch.cuda.empty_cache()
+
     return res
 
 
@@ -656,8 +677,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip secondary workloads; short CPU baseline")
-    ap.add_argument("--legs", default="gather,long,mtp,tiny,qlen1,sweep,mxfp8",
-                    help="secondary workloads to time (comma list of gather, long, mtp, tiny, qlen1, sweep, mxfp8; "
+    ap.add_argument("--legs", default="gather,long,mtp,prefill,tiny,qlen1,sweep,mxfp8",
+                    help="secondary workloads to time (comma list of gather, long, mtp, prefill, tiny, qlen1, sweep, mxfp8; "
                          "empty for none)")
     args = ap.parse_args()
     args.legs = set() if args.quick else {x for x in args.legs.split(",") if x}

@@ -19,7 +19,8 @@
  *     library never allocates, frees or synchronises; it only enqueues
  *     kernels on `stream` (a cudaStream_t; NULL = the legacy default stream),
  *     so idx_dequant_nvfp4_pages, idx_score_pages, idx_topk16_select,
- *     idx_decode_step and idx_mtp_score_fp8 can sit inside CUDA-graph capture.
+ *     idx_decode_step, idx_mtp_score_fp8, idx_prefill_index_step and
+ *     idx_mxfp8_quantize can sit inside CUDA-graph capture.
  *   - Return value: IDX_OK (0) when the work was enqueued (or there was
  *     nothing to do), else a negative IDX_E_* code; on an error nothing is
  *     launched.  Argument checks are on the host and never touch the GPU.
@@ -257,6 +258,59 @@ int idx_mtp_score_fp8(const uint8_t* q, const float* q_scale, int32_t num_tokens
                       const uint8_t* k, const float* k_scale, int64_t num_blocks, const int32_t* block_table,
                       int64_t bt_stride, int32_t max_blocks, const int32_t* num_keys, const int32_t* cu_tokens,
                       int32_t num_reqs, int32_t max_keys, float* out, int32_t* status, void* stream);
+
+/*
+ * Q8KV8 prefill indexer chain over NVFP4 index-K pages ([GATHER] module
+ * docstring: the gathered, dequantised pages feed the Q8KV8 prefill indexer;
+ * [MTP] prefill / causal masking and the -inf tail-fill fusion; [PUBLISH]
+ * the prefill top-k).  With nk_r = clamp(num_keys[r], 0, min(max_keys,
+ * max_blocks * 128)) and token t the i-th of request r's n_r tokens, at
+ * position pos_t = num_keys[r] - n_r + i:
+ *     scores[t][key] = sum_h relu(q[t][h] . K_r[key]) * q_scale[t][h]
+ *                                             for key <= pos_t, key < nk_r,
+ *                    = -inf                   for pos_t < key < nk_r and for
+ *                                             nk_r <= key < max_keys,
+ *                    = NaN                    for a key of a page whose block
+ *                                             id is outside [0, num_blocks)
+ *                                             (IDX_ST_BLOCK_OOR; -inf where
+ *                                             masked),
+ * K_r[key] being key % 128 of page block_table[r][key / 128] dequantised
+ * exactly as in idx_dequant_nvfp4_pages; and
+ *     out[t] = the 16 best keys of [0, visible_t), visible_t = clamp(pos_t + 1,
+ *              0, nk_r), in idx_topk16_select's order (score descending, NaN
+ *              ranked as -inf, equal scores by lower key), padded with -1.
+ *
+ *   kv, num_blocks, block_table, bt_stride, max_blocks
+ *                 as in idx_dequant_nvfp4_pages; row r's first
+ *                 ceil(nk_r / 128) entries are read.
+ *   num_keys      [num_reqs] int32 keys of request r, its new tokens included.
+ *   cu_tokens     [num_reqs + 1] int32, non-decreasing, cu_tokens[0] = 0 and
+ *                 cu_tokens[num_reqs] = num_tokens; tokens outside every
+ *                 request get a row of -inf and no keys.
+ *   q             [num_tokens, heads, 128] E4M3 bytes, 16-byte aligned;
+ *                 heads in [1, 128] (64 runs on the tensor cores).
+ *   q_scale       [num_tokens, heads] float32 (16-byte aligned for the
+ *                 tensor-core scorer).
+ *   scores        [num_tokens, max_keys] float32, every element written.
+ *   out           [num_tokens, 16] int32.
+ *   workspace     idx_prefill_workspace_bytes(...) bytes, 256-byte aligned,
+ *                 no initialisation needed: the dequantised pages
+ *                 (num_reqs * min(max_blocks, ceil(max_keys / 128)) pages of
+ *                 16,384 bytes), their block table, per-token visible counts
+ *                 and the selector's workspace.
+ * Accumulation in fp32; a score is within 1e-3 * sum_h |q_scale_h| sum_d
+ * |q_hd k_d| of the exact value.  IDX_E_WORKSPACE when workspace_bytes is
+ * short; IDX_E_TOO_LARGE when the pages would pass 2^31 keys.
+ *
+ * idx_prefill_workspace_bytes: the workspace size for these sizes (0 for a
+ * negative size).
+ */
+size_t idx_prefill_workspace_bytes(int32_t num_reqs, int32_t max_blocks, int32_t num_tokens, int32_t max_keys);
+int idx_prefill_index_step(const uint8_t* kv, int64_t num_blocks, const int32_t* block_table, int64_t bt_stride,
+                           int32_t max_blocks, const int32_t* num_keys, const int32_t* cu_tokens, int32_t num_reqs,
+                           const uint8_t* q, const float* q_scale, int32_t num_tokens, int32_t heads,
+                           int32_t max_keys, float* scores, int32_t* out, void* workspace, size_t workspace_bytes,
+                           int32_t* status, void* stream);
 
 /*
  * MXFP8 quantisation of bf16 rows ("vLLM PR #65508", the description of the

@@ -390,7 +390,7 @@ def prefill_positions(num_keys, cu_tokens) -> np.ndarray:
     return pos
 
 
-def prefill_step(kv, bt, num_keys, cu_tokens, q, q_scale, max_keys):
+def prefill_step(kv, bt, num_keys, cu_tokens, q, q_scale, max_keys, tokens=None):
     """The Q8KV8 prefill indexer chain, stated plainly.
 
     * Gather and dequantise each request's NVFP4 index-K pages to E4M3
@@ -407,16 +407,22 @@ def prefill_step(kv, bt, num_keys, cu_tokens, q, q_scale, max_keys):
       top-k promises cutoff ties to the lower id, matching the merge), -1 pad.
 
     Returns (scores [T, max_keys] f32, bound [T, max_keys] f64, visible [T],
-    out [T, 16] int32, status).
+    out [T, 16] int32, status); with ``tokens`` (a list of token ids) only
+    those rows, in that order, and only the pages of their requests.
     """
     kv = np.asarray(kv).reshape(-1, PAGE_BYTES)
     T = int(cu_tokens[-1])
-    scores = np.full((T, max_keys), -np.inf, dtype=np.float32)
-    bound = np.zeros((T, max_keys), dtype=np.float64)
+    rows = list(range(T)) if tokens is None else [int(t) for t in tokens]
+    row_of = {t: i for i, t in enumerate(rows)}
+    scores = np.full((len(rows), max_keys), -np.inf, dtype=np.float32)
+    bound = np.zeros((len(rows), max_keys), dtype=np.float64)
     pos = prefill_positions(num_keys, cu_tokens)
-    visible = np.zeros(T, dtype=np.int64)
+    visible = np.zeros(len(rows), dtype=np.int64)
     status = 0
     for r in range(len(num_keys)):
+        mine = [t for t in range(int(cu_tokens[r]), int(cu_tokens[r + 1])) if t in row_of]
+        if not mine:
+            continue
         nk = max(0, min(int(num_keys[r]), int(max_keys), bt.shape[1] * PAGE_TOKENS))
         npg = -(-nk // PAGE_TOKENS)
         keys = np.zeros((npg * PAGE_TOKENS, HEAD_DIM), dtype=np.uint8)
@@ -428,17 +434,18 @@ def prefill_step(kv, bt, num_keys, cu_tokens, q, q_scale, max_keys):
             else:
                 status |= ST_BLOCK_OOR
                 valid[p * PAGE_TOKENS:(p + 1) * PAGE_TOKENS] = False
-        for t in range(int(cu_tokens[r]), int(cu_tokens[r + 1])):
-            visible[t] = max(0, min(int(pos[t]) + 1, nk))
+        for t in mine:
+            i = row_of[t]
+            visible[i] = max(0, min(int(pos[t]) + 1, nk))
             if nk == 0:
                 continue
             s, b = mtp_token_scores(q[t], q_scale[t], keys[:nk], np.ones(nk, dtype=np.float32))
             cols = np.arange(nk)
             keep = cols <= pos[t]
             s = np.where(valid[:nk], s, np.float32(np.nan))
-            scores[t, :nk] = np.where(keep, s, np.float32(-np.inf))
-            bound[t, :nk] = np.where(keep & valid[:nk], b, 0.0)
-    out = np.full((T, TOPK), -1, dtype=np.int32)
-    for t in range(T):
-        out[t], _ = top16(scores[t], int(visible[t]))
+            scores[i, :nk] = np.where(keep, s, np.float32(-np.inf))
+            bound[i, :nk] = np.where(keep & valid[:nk], b, 0.0)
+    out = np.full((len(rows), TOPK), -1, dtype=np.int32)
+    for i in range(len(rows)):
+        out[i], _ = top16(scores[i], int(visible[i]))
     return scores, bound, visible, out, status

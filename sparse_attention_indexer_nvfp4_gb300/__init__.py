@@ -31,6 +31,8 @@ __all__ = [
     "idx_decode_step",
     "RANK_16BIT",
     "idx_mtp_score_fp8",
+    "idx_prefill_workspace_bytes",
+    "idx_prefill_index_step",
     "idx_mxfp8_quantize",
     "SYMBOLS",
     "ST_BLOCK_OOR",
@@ -47,8 +49,8 @@ ST_BLOCK_OOR = 1
 ST_LEN_CLAMPED = 2
 ST_BAD_OUTPUT = 4
 ST_TIMEOUT = 8
-NOALLOC_SCRATCH_BYTES = 4 << 20
-DEFAULT_WAIT_POLLS = 100_000  # pipeline-wait budget of the tensor-core kernels (about 2 s)  # scratch inside the library used by idx_topk16_select_noalloc
+NOALLOC_SCRATCH_BYTES = 4 << 20  # scratch inside the library used by idx_topk16_select_noalloc
+DEFAULT_WAIT_POLLS = 100_000  # pipeline-wait budget of the tensor-core kernels (about 2 s)
 
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -69,6 +71,9 @@ SYMBOLS = {
     "idx_decode_step": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p, _sz, _i32, _p,
                                        _p]),
     "idx_mtp_score_fp8": (ctypes.c_int, [_p, _p, _i32, _i32, _p, _p, _i64, _p, _i64, _i32, _p, _p, _i32, _i32, _p, _p, _p]),
+    "idx_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
+    "idx_prefill_index_step": (ctypes.c_int, [_p, _i64, _p, _i64, _i32, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _p, _p,
+                                              _p, _sz, _p, _p]),
     "idx_mxfp8_quantize": (ctypes.c_int, [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p]),
 }
 
@@ -226,6 +231,22 @@ def idx_mtp_score_fp8(q, q_scale, k, k_scale, block_table, num_keys, cu_tokens, 
         _ptr(q), _ptr(q_scale), q.shape[0], q.shape[1], _ptr(k), _ptr(k_scale), k.shape[0], _ptr(block_table),
         _row_stride(block_table), block_table.shape[1], _ptr(num_keys), _ptr(cu_tokens), num_keys.shape[0],
         int(max_keys), _ptr(out), _ptr(status), _stream(stream)))
+
+
+def idx_prefill_workspace_bytes(num_reqs: int, max_blocks: int, num_tokens: int, max_keys: int) -> int:
+    return int(load_library().idx_prefill_workspace_bytes(num_reqs, max_blocks, num_tokens, max_keys))
+
+
+def idx_prefill_index_step(kv, block_table, num_keys, cu_tokens, q, q_scale, max_keys: int, scores, out, workspace,
+                           status=None, stream=None) -> int:
+    """Prefill chain: kv [nb,128,72] u8 NVFP4 pages; q [T,H,128] e4m3; scores [T,max_keys] f32; out [T,16] i32;
+    workspace of idx_prefill_workspace_bytes(...) bytes."""
+    lib = load_library()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    return _check("idx_prefill_index_step", lib.idx_prefill_index_step(
+        _ptr(kv), kv.shape[0], _ptr(block_table), _row_stride(block_table), block_table.shape[1], _ptr(num_keys),
+        _ptr(cu_tokens), num_keys.shape[0], _ptr(q), _ptr(q_scale), q.shape[0], q.shape[1], int(max_keys),
+        _ptr(scores), _ptr(out), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
 
 
 def idx_mxfp8_quantize(x, out, scales, stream=None) -> int:

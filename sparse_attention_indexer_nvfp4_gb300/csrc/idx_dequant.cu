@@ -81,6 +81,18 @@ __global__ void __launch_bounds__(kDqThreads) k_dequant_nvfp4(const uint8_t* __r
 }
 
 }  // namespace
+
+int launch_dequant(const uint8_t* kv, int64_t num_blocks, const int32_t* bt, int64_t bt_stride, int32_t max_blocks,
+                   const int32_t* num_pages, const int32_t* page_offsets, int32_t num_reqs, int32_t max_num_pages,
+                   uint8_t* out, int64_t out_pages, int32_t* status, cudaStream_t stream) {
+  const int64_t items = (int64_t)num_reqs * (int64_t)max_num_pages;
+  if (items > 0x7FFFFFFFLL) return IDX_E_TOO_LARGE;
+  if (items == 0) return IDX_OK;
+  launch_pdl(k_dequant_nvfp4, dim3((unsigned)items), dim3(kDqThreads), 0, stream, kv, num_blocks, bt, bt_stride,
+             max_blocks, num_pages, page_offsets, max_num_pages, out, out_pages, status);
+  return launch_result();
+}
+
 }  // namespace idx
 
 extern "C" int idx_have_qmul4(void) { return IDX_HAVE_QMUL4 ? 1 : 0; }
@@ -97,12 +109,9 @@ extern "C" int idx_dequant_nvfp4_pages(const uint8_t* kv, int64_t num_blocks, co
   if (!aligned(kv, 16) || !aligned(out, 16) || !aligned(block_table, 4) || !aligned(num_pages, 4) ||
       !aligned(page_offsets, 4))
     return IDX_E_MISALIGNED;
-  const int64_t items = (int64_t)num_reqs * (int64_t)max_num_pages;
-  if (items > 0x7FFFFFFFLL) return IDX_E_TOO_LARGE;
+  if ((int64_t)num_reqs * (int64_t)max_num_pages > 0x7FFFFFFFLL) return IDX_E_TOO_LARGE;
   int rc = check_device();
   if (rc != IDX_OK) return rc;
-  launch_pdl(k_dequant_nvfp4, dim3((unsigned)items), dim3(kDqThreads), 0, (cudaStream_t)stream,
-      kv, num_blocks, block_table, bt_stride, max_blocks, num_pages, page_offsets, max_num_pages, out, out_pages,
-      status);
-  return launch_result();
+  return launch_dequant(kv, num_blocks, block_table, bt_stride, max_blocks, num_pages, page_offsets, num_reqs,
+                        max_num_pages, out, out_pages, status, (cudaStream_t)stream);
 }

@@ -116,12 +116,26 @@ int launch_topk_plain(const float* scores, int64_t row_stride, int32_t rows, int
 
 int launch_topk_decode(const DecodeRows& d, void* ws, cudaStream_t stream);
 
+constexpr int kMtpMaxHeads = 128;  // head limit of the multi-token scorers
+
 // Multi-token scorer on the tensor cores (64 heads); see mtp_tc_supported for the shapes it takes.
 bool mtp_tc_supported(const uint8_t* q, const float* q_scale, const uint8_t* k, const float* k_scale, int32_t heads,
                       int32_t num_tokens, int64_t num_blocks);
+// prefill != 0: causal mask (token t of request r at position
+// num_keys[r] - ntok + (t - tok0) sees keys up to it; the others score -inf) and a key
+// of a block outside the pool scores NaN.  k_scale may be NULL (scales of 1).
 int launch_mtp_tc(const uint8_t* q, const float* q_scale, int32_t num_tokens, const uint8_t* k, const float* k_scale,
                   int64_t num_blocks, const int32_t* bt, int64_t bt_stride, int32_t max_blocks, const int32_t* num_keys,
                   const int32_t* cu_tokens, int32_t num_reqs, int32_t max_keys, float* out, int32_t* status,
-                  cudaStream_t stream);
+                  cudaStream_t stream, int32_t prefill);
+// Multi-token scorer on the CUDA cores (any head count up to 128), same arguments.
+int launch_mtp_fma(const uint8_t* q, const float* q_scale, int32_t num_tokens, int32_t heads, const uint8_t* k,
+                   const float* k_scale, int64_t num_blocks, const int32_t* bt, int64_t bt_stride, int32_t max_blocks,
+                   const int32_t* num_keys, const int32_t* cu_tokens, int32_t num_reqs, int32_t max_keys, float* out,
+                   int32_t* status, cudaStream_t stream, int32_t prefill);
+// Gather + dequantise NVFP4 pages (the idx_dequant_nvfp4_pages kernel).
+int launch_dequant(const uint8_t* kv, int64_t num_blocks, const int32_t* bt, int64_t bt_stride, int32_t max_blocks,
+                   const int32_t* num_pages, const int32_t* page_offsets, int32_t num_reqs, int32_t max_num_pages,
+                   uint8_t* out, int64_t out_pages, int32_t* status, cudaStream_t stream);
 
 }  // namespace idx

@@ -15,8 +15,8 @@ namespace {
 
 constexpr int kMtpThreads = 128;
 constexpr int kKPad = kHeadDim + 1;
-constexpr int kMaxHeads = 128;
-constexpr size_t kMtpSmem = sizeof(float) * (kPageTokens * kKPad + kMaxHeads * kHeadDim + kMaxHeads);
+
+constexpr size_t kMtpSmem = sizeof(float) * (kPageTokens * kKPad + kMtpMaxHeads * kHeadDim + kMtpMaxHeads);
 
 __global__ void __launch_bounds__(kMtpThreads) k_mtp_fma(const uint8_t* __restrict__ q, const float* __restrict__ q_scale,
                                                          int32_t heads, const uint8_t* __restrict__ k,
@@ -24,27 +24,33 @@ __global__ void __launch_bounds__(kMtpThreads) k_mtp_fma(const uint8_t* __restri
                                                          const int32_t* __restrict__ bt, int64_t bt_stride,
                                                          int32_t max_blocks, const int32_t* __restrict__ num_keys,
                                                          const int32_t* __restrict__ cu_tokens, int32_t num_tokens,
-                                                         int32_t max_keys, float* __restrict__ out, int32_t* status) {
+                                                         int32_t max_keys, float* __restrict__ out, int32_t* status,
+                                                         int32_t prefill) {
   pdl_enter();  // before any global-memory access
   extern __shared__ float smem[];
   float* kf = smem;                              // [128][129]
   float* qf = kf + kPageTokens * kKPad;          // [heads][128]
-  float* qsf = qf + kMaxHeads * kHeadDim;        // [heads]
+  float* qsf = qf + kMtpMaxHeads * kHeadDim;        // [heads]
   const int kt = blockIdx.x, r = blockIdx.y;
   const int nk = max(0, min(num_keys[r], min(max_keys, max_blocks * kPageTokens)));
   const int key0 = kt * kPageTokens;
   if (key0 >= nk) return;
   const int tid = threadIdx.x;
   const int64_t blk = bt[(int64_t)r * bt_stride + kt];
+  const int t0 = max(0, cu_tokens[r]), t1 = min(num_tokens, cu_tokens[r + 1]);
+  const bool live = key0 + tid < nk;
+  // prefill: token t at position num_keys - (t1 - t0) + (t - t0) sees keys up to it (causal mask)
+  auto masked = [&](int t) { return prefill && key0 + tid > num_keys[r] - (t1 - t0) + (t - t0); };
   if (blk < 0 || blk >= num_blocks) {
     if (tid == 0) report(status, IDX_ST_BLOCK_OOR);
+    if (prefill && live)  // a key of a block outside the pool scores NaN (-inf where masked)
+      for (int t = t0; t < t1; ++t)
+        out[(int64_t)t * max_keys + key0 + tid] = masked(t) ? -INFINITY : __int_as_float(0x7FC00000);
     return;
   }
   const uint8_t* kb = k + blk * (int64_t)(kPageTokens * kHeadDim);
   for (int e = tid; e < kPageTokens * kHeadDim; e += kMtpThreads) kf[(e >> 7) * kKPad + (e & 127)] = e4m3_to_f32(kb[e]);
-  const float ks = k_scale[blk * kPageTokens + tid];
-  const int t0 = max(0, cu_tokens[r]), t1 = min(num_tokens, cu_tokens[r + 1]);
-  const bool live = key0 + tid < nk;
+  const float ks = k_scale != nullptr ? k_scale[blk * kPageTokens + tid] : 1.f;
   for (int t = t0; t < t1; ++t) {
     __syncthreads();
     const uint8_t* qt = q + (int64_t)t * heads * kHeadDim;
@@ -58,7 +64,7 @@ __global__ void __launch_bounds__(kMtpThreads) k_mtp_fma(const uint8_t* __restri
       for (int d = 0; d < kHeadDim; ++d) dot = fmaf(qf[h * kHeadDim + d], kf[tid * kKPad + d], dot);
       total = fmaf(fmaxf(dot, 0.f), qsf[h], total);
     }
-    if (live) out[(int64_t)t * max_keys + key0 + tid] = total * ks;
+    if (live) out[(int64_t)t * max_keys + key0 + tid] = masked(t) ? -INFINITY : total * ks;
   }
 }
 
@@ -67,14 +73,14 @@ __global__ void __launch_bounds__(kMtpThreads) k_mtp_fma(const uint8_t* __restri
 int launch_mtp_fma(const uint8_t* q, const float* q_scale, int32_t num_tokens, int32_t heads, const uint8_t* k,
                    const float* k_scale, int64_t num_blocks, const int32_t* bt, int64_t bt_stride, int32_t max_blocks,
                    const int32_t* num_keys, const int32_t* cu_tokens, int32_t num_reqs, int32_t max_keys, float* out,
-                   int32_t* status, cudaStream_t stream) {
+                   int32_t* status, cudaStream_t stream, int32_t prefill) {
   if (cudaFuncSetAttribute(k_mtp_fma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMtpSmem) != cudaSuccess)
     return IDX_E_CUDA;
   const int tiles = (min(max_keys, max_blocks * kPageTokens) + kPageTokens - 1) / kPageTokens;
   if (tiles <= 0) return IDX_OK;
   launch_pdl(k_mtp_fma, dim3((unsigned)tiles, (unsigned)num_reqs), dim3(kMtpThreads), kMtpSmem, stream,
       q, q_scale, heads, k, k_scale, num_blocks, bt, bt_stride, max_blocks, num_keys, cu_tokens, num_tokens, max_keys, out,
-      status);
+      status, prefill);
   return launch_result();
 }
 
@@ -88,7 +94,7 @@ extern "C" int idx_mtp_score_fp8(const uint8_t* q, const float* q_scale, int32_t
   using namespace idx;
   if (num_tokens < 0 || num_reqs < 0 || max_keys < 0 || max_blocks < 0 || num_blocks < 0 || bt_stride < 0)
     return IDX_E_BAD_SHAPE;
-  if (heads < 1 || heads > kMaxHeads) return IDX_E_BAD_SHAPE;
+  if (heads < 1 || heads > kMtpMaxHeads) return IDX_E_BAD_SHAPE;
   if (num_reqs == 0 || num_tokens == 0 || max_keys == 0 || max_blocks == 0) return IDX_OK;
   if (num_reqs > 65535) return IDX_E_TOO_LARGE;
   if (!q || !q_scale || !k || !k_scale || !block_table || !num_keys || !cu_tokens || !out) return IDX_E_NULL_PTR;
@@ -100,7 +106,7 @@ extern "C" int idx_mtp_score_fp8(const uint8_t* q, const float* q_scale, int32_t
   if (rc != IDX_OK) return rc;
   if (mtp_tc_supported(q, q_scale, k, k_scale, heads, num_tokens, num_blocks))
     return launch_mtp_tc(q, q_scale, num_tokens, k, k_scale, num_blocks, block_table, bt_stride, max_blocks, num_keys,
-                         cu_tokens, num_reqs, max_keys, out, status, (cudaStream_t)stream);
+                         cu_tokens, num_reqs, max_keys, out, status, (cudaStream_t)stream, 0);
   return launch_mtp_fma(q, q_scale, num_tokens, heads, k, k_scale, num_blocks, block_table, bt_stride, max_blocks, num_keys,
-                        cu_tokens, num_reqs, max_keys, out, status, (cudaStream_t)stream);
+                        cu_tokens, num_reqs, max_keys, out, status, (cudaStream_t)stream, 0);
 }

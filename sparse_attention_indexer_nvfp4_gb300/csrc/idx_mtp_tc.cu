@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
                                                       const float* __restrict__ k_scale, int64_t num_blocks,
                                                       const int32_t* __restrict__ bt, int64_t bt_stride,
                                                       ReqShape shape, int32_t max_keys, float* __restrict__ out,
-                                                      int32_t* status, uint32_t wait_polls) {
+                                                      int32_t* status, uint32_t wait_polls, int32_t prefill) {
   pdl_enter();  // before any global-memory access
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -248,8 +248,12 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
             if (valid) {
               mbar_arrive_expect_tx(&bars[kKFull + stage], kKTileBytes);
               tma_load_2d(smem + kOffKm + stage * kKTileBytes, &kmap, 0, (int)(blk * kPageTokens), &bars[kKFull + stage]);
-              mbar_arrive_expect_tx(&bars[kKsFull + ks], kKsBytes);
-              bulk_g2s(smem + kOffKs + ks * kKsBytes, k_scale + blk * kPageTokens, kKsBytes, &bars[kKsFull + ks]);
+              if (k_scale != nullptr) {
+                mbar_arrive_expect_tx(&bars[kKsFull + ks], kKsBytes);
+                bulk_g2s(smem + kOffKs + ks * kKsBytes, k_scale + blk * kPageTokens, kKsBytes, &bars[kKsFull + ks]);
+              } else {
+                mbar_arrive(&bars[kKsFull + ks]);  // no per-key scales: 1
+              }
             } else {
               report(status, IDX_ST_BLOCK_OOR);
               mbar_arrive(&bars[kKFull + stage]);
@@ -331,7 +335,8 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
         if (!__all_sync(0xFFFFFFFFu, ks_ok && acc_ok)) break;
       }
       tc_fence_after();
-      const float ks = reinterpret_cast<const float*>(smem + kOffKs + slot * kKsBytes)[quarter * 32 + lane];
+      const float ks =
+          k_scale != nullptr ? reinterpret_cast<const float*>(smem + kOffKs + slot * kKsBytes)[quarter * 32 + lane] : 1.f;
       const bool valid = valid_ring[slot] != 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kKsEmpty + slot]);
@@ -367,9 +372,21 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
         }
       }
       const int key = kb * kPageTokens + quarter * 32 + lane;
-      if (valid && key < shape.nk(r)) {
-        out[(int64_t)t0 * max_keys + key] = ((part[0][0] + part[0][1]) + (part[0][2] + part[0][3])) * ks;
-        if (nt > 1) out[(int64_t)(t0 + 1) * max_keys + key] = ((part[1][0] + part[1][1]) + (part[1][2] + part[1][3])) * ks;
+      if (key < shape.nk(r)) {
+        float v0 = ((part[0][0] + part[0][1]) + (part[0][2] + part[0][3])) * ks;
+        float v1 = ((part[1][0] + part[1][1]) + (part[1][2] + part[1][3])) * ks;
+        if (prefill) {
+          // causal mask: token t at position num_keys - ntok + (t - tok0) sees keys up
+          // to it; a key of a block outside the pool scores NaN
+          const int pos0 = shape.num_keys[r] - shape.ntok(r) + (t0 - shape.tok0(r));
+          if (!valid) v0 = v1 = __int_as_float(0x7FC00000);
+          if (key > pos0) v0 = -INFINITY;
+          if (key > pos0 + 1) v1 = -INFINITY;
+        }
+        if (valid || prefill) {
+          out[(int64_t)t0 * max_keys + key] = v0;
+          if (nt > 1) out[(int64_t)(t0 + 1) * max_keys + key] = v1;
+        }
       }
     }
   }
@@ -406,7 +423,7 @@ bool mtp_tc_supported(const uint8_t* q, const float* q_scale, const uint8_t* k, 
 int launch_mtp_tc(const uint8_t* q, const float* q_scale, int32_t num_tokens, const uint8_t* k, const float* k_scale,
                   int64_t num_blocks, const int32_t* bt, int64_t bt_stride, int32_t max_blocks, const int32_t* num_keys,
                   const int32_t* cu_tokens, int32_t num_reqs, int32_t max_keys, float* out, int32_t* status,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, int32_t prefill) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IDX_E_CUDA;
   if (!g_attr_m[dev]) {
@@ -425,7 +442,7 @@ int launch_mtp_tc(const uint8_t* q, const float* q_scale, int32_t num_tokens, co
   // two CTAs per SM: 256 TMEM columns and ~100 KB of shared memory each
   const int grid = 2 * g_sms_m[dev];
   launch_pdl(k_mtp_tc, dim3(grid), dim3(kThreadsM), kSmemM, stream, kmap, qmap, q_scale, k_scale, num_blocks, bt, bt_stride, sh, max_keys,
-                                                 out, status, wait_polls());
+                                                 out, status, wait_polls(), prefill);
   return launch_result();
 }
 

@@ -17,6 +17,9 @@ Every array is numpy; sizes follow the workloads described by the pages:
 * Multi-token scorer, "Mojo sparse_index_fp8_sm100" module text:
   Q [tokens, heads, 128] E4M3, paged K [keys, 128] E4M3 with a per-key
   fp32 k_scale.
+* Chunked prefill, "Mojo sparse_index_fp8_sm100" (prefill / causal masking):
+  each request's new tokens are the last keys of its context, NVFP4 pages as
+  above, Q [tokens, heads, 128] E4M3.
 * The top-16 stress rows of the "MSA PR #1" test description: widths from a
   few columns to thousands, with injected +-inf, NaN, +-0 and FLT_MAX.
 
@@ -220,6 +223,41 @@ def mtp_workload(seed: int = 3, num_reqs: int = 32, tokens_per_req: int = 2, hea
     q_scale = random_uniform_f32(rng, (T, heads), 0.5, 2.0)
     return dict(q=q, q_scale=q_scale, k=k, k_scale=k_scale, bt=bt, num_keys=num_keys, cu_tokens=cu_tokens,
                 max_keys=int(num_keys.max()) if num_reqs else 0, num_blocks=num_blocks, heads=heads)
+
+
+# ---------------------------------------------------------------------------
+# prefill chain workload
+# ---------------------------------------------------------------------------
+
+def prefill_workload(seed: int = 5, num_keys=(16384, 16384, 16384, 16384), new_tokens=(2048, 2048, 2048, 2048),
+                     heads: int = 64, spare_blocks: int = 8, max_keys: int | None = None) -> dict:
+    """Chunked prefill over NVFP4 index-K pages: request r holds num_keys[r]
+    keys, the last new_tokens[r] of which are this chunk's tokens (scored
+    with the causal mask); each request's pages are distinct blocks of one
+    shuffled pool, with a few spare blocks that no request uses."""
+    rng = rng_for(seed)
+    num_keys = np.asarray(num_keys, dtype=np.int32)
+    new_tokens = np.asarray(new_tokens, dtype=np.int32)
+    R = len(num_keys)
+    pages = np.array([pages_for_len(int(n)) for n in num_keys], dtype=np.int64)
+    max_blocks = int(max(1, pages.max())) if R else 1
+    num_blocks = int(pages.sum()) + spare_blocks
+    kv = random_nvfp4_pages(rng, num_blocks)
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    bt = np.zeros((R, max_blocks), dtype=np.int32)
+    off = 0
+    for r in range(R):
+        n = int(pages[r])
+        bt[r, :n] = perm[off:off + n]
+        off += n
+    cu_tokens = np.concatenate([[0], np.cumsum(new_tokens)]).astype(np.int32)
+    T = int(cu_tokens[-1])
+    q = random_e4m3(rng, (T, heads, HEAD_DIM))
+    q_scale = random_uniform_f32(rng, (T, heads), 0.5, 2.0)
+    if max_keys is None:
+        max_keys = int(num_keys.max()) if R else 0
+    return dict(kv=kv, bt=bt, num_keys=num_keys, cu_tokens=cu_tokens, q=q, q_scale=q_scale, max_keys=int(max_keys),
+                num_blocks=num_blocks, heads=heads)
 
 
 # ---------------------------------------------------------------------------

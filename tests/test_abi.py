@@ -114,3 +114,20 @@ def test_qmul4_flag_matches_probe(built):
     from sparse_attention_indexer_nvfp4_gb300 import build
 
     assert built.idx_have_qmul4() == build.probe_qmul4()
+
+
+def test_prefill_workspace_sizing_and_checks(built):
+    lib = built.load_library()
+    # 3 requests x min(10 blocks, ceil(1000 / 128) = 8) pages of 16,384 bytes come first
+    n = built.idx_prefill_workspace_bytes(3, 10, 50, 1000)
+    assert n >= 3 * 8 * 16384 + 3 * 8 * 4 + 50 * 4 and n % 256 == 0
+    assert built.idx_prefill_workspace_bytes(3, 10, 50, 100_000) >= 3 * 10 * 16384
+    assert built.idx_prefill_workspace_bytes(-1, 10, 50, 1000) == 0
+    E_NULL, E_SHAPE, E_MIS, E_WS = -1, -2, -3, -7
+    a = 4096  # a 256-byte aligned stand-in address: these checks answer before any CUDA call
+    args = [a, 10, a, 10, 10, a, a, 3, a, a, 50, 64, 1000, a, a, a, n, None, None]
+    for i, v, want in [(11, 0, E_SHAPE), (11, 129, E_SHAPE), (16, n - 1, E_WS), (15, a + 16, E_MIS),
+                       (15, None, E_NULL), (3, 4, E_SHAPE), (10, 0, 0)]:
+        bad = list(args)
+        bad[i] = v
+        assert lib.idx_prefill_index_step(*bad) == want, (i, v)

@@ -57,3 +57,13 @@ def test_bad_block_scores_nan():
     s, _, _, _, st = prefill_step(kv, bt, nk, cu, q, qs, 320)
     assert st & 1
     assert np.isnan(s[2, 128:256]).all() and np.isfinite(s[2, :128]).all()
+
+
+def test_token_subset_equals_full_rows():
+    kv, bt, nk, cu, q, qs = _case()
+    full = prefill_step(kv, bt, nk, cu, q, qs, 320)
+    pick = [5, 0, 7, 2]
+    part = prefill_step(kv, bt, nk, cu, q, qs, 320, tokens=pick)
+    for a, b in zip(part[:4], full[:4]):
+        assert np.array_equal(a, b[pick], equal_nan=True)
+    assert part[4] == full[4]
