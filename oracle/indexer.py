@@ -21,7 +21,11 @@ q_scale * (q . k) in fp32 (the dot rounded once to fp32, then one fp32
 multiply); page bytes are all 8,192 code bytes, then the 1,024 scale bytes
 at 8192 + token * 8 + group, group = element // 16; a NaN scale dequantises
 to 0x7F; the page field of a key is 32 bits wide; a page whose block id is
-out of range scores NaN (ranked as -inf) and raises a status bit.
+out of range scores NaN (ranked as -inf) and raises a status bit.  P256
+pages ("wolfcomos/MSA PR #1", Performance: P128 and P256 pages, 672-column
+rows at 168K tokens) keep the same per-token layout over 256 tokens: the
+16,384 code bytes of all tokens, then the 2,048 scale bytes, 18,432 bytes a
+page; own page, scored pages and the page reduction count 256 keys a page.
 """
 
 from __future__ import annotations
@@ -50,29 +54,35 @@ ST_BAD_OUTPUT = 4  # an output page index outside the output buffer: skipped
 # NVFP4 pages
 # ---------------------------------------------------------------------------
 
-def page_fields(page: np.ndarray):
-    """Split one packed page into E2M1 codes [128, 128] and E4M3 scales [128, 8].
+def page_bytes(page_tokens: int = PAGE_TOKENS) -> int:
+    """Bytes of one packed page: 64 code bytes and 8 scale bytes per token."""
+    return page_tokens * (HEAD_DIM // 2 + HEAD_DIM // 16)
+
+
+def page_fields(page: np.ndarray, page_tokens: int = PAGE_TOKENS):
+    """Split one packed page into E2M1 codes [T, 128] and E4M3 scales [T, 8], T = page_tokens.
 
     Token t's 64 code bytes start at t * 64; element d sits in byte
     t * 64 + d // 2, low nibble for even d, high nibble for odd d.  The
-    scales follow all codes: scale (t, g) at byte 8192 + t * 8 + g.
+    scales follow all codes: scale (t, g) at byte T * 64 + t * 8 + g.
     """
-    flat = np.asarray(page, dtype=np.uint8).reshape(PAGE_BYTES)
-    code_bytes = flat[:CODE_BYTES].reshape(PAGE_TOKENS, HEAD_DIM // 2)
-    codes = np.empty((PAGE_TOKENS, HEAD_DIM), dtype=np.uint8)
+    code_end = page_tokens * HEAD_DIM // 2
+    flat = np.asarray(page, dtype=np.uint8).reshape(page_bytes(page_tokens))
+    code_bytes = flat[:code_end].reshape(page_tokens, HEAD_DIM // 2)
+    codes = np.empty((page_tokens, HEAD_DIM), dtype=np.uint8)
     codes[:, 0::2] = code_bytes & 0x0F
     codes[:, 1::2] = code_bytes >> 4
-    scales = flat[CODE_BYTES:].reshape(PAGE_TOKENS, HEAD_DIM // 16)
+    scales = flat[code_end:].reshape(page_tokens, HEAD_DIM // 16)
     return codes, scales
 
 
-def dequant_page(page: np.ndarray) -> np.ndarray:
-    """[128, 128] E4M3 bytes: e4m3_rn_satfinite(e2m1(code) * e4m3(scale)).
+def dequant_page(page: np.ndarray, page_tokens: int = PAGE_TOKENS) -> np.ndarray:
+    """[page_tokens, 128] E4M3 bytes: e4m3_rn_satfinite(e2m1(code) * e4m3(scale)).
 
     The product of an E2M1 value (at most 2 significant bits) and an E4M3
     value (at most 4) is exact in float64; ``e4m3_encode`` rounds it once.
     """
-    codes, scales = page_fields(page)
+    codes, scales = page_fields(page, page_tokens)
     group_scale = scales[:, np.arange(HEAD_DIM) // 16]
     x = E2M1_VALUES[codes] * E4M3_VALUES[group_scale]
     return e4m3_encode(x)
@@ -121,10 +131,10 @@ def e4m3_units(b: np.ndarray) -> np.ndarray:
 
 
 def page_scores(q_rows: np.ndarray, q_scale: np.ndarray, kdeq: np.ndarray) -> np.ndarray:
-    """Score of one page for each query row: max over the 128 keys of
+    """Score of one page for each query row: max over the page's keys of
     fp32(q_scale * fp32(q . k)).
 
-    q_rows [R, 128] E4M3 bytes, q_scale [R] float32, kdeq [128, 128] E4M3
+    q_rows [R, 128] E4M3 bytes, q_scale [R] float32, kdeq [T, 128] E4M3
     bytes (token, depth).  The dot is exact in int64 (units of 2^-18), then
     rounded once to fp32 and multiplied by q_scale in fp32.
     """
@@ -144,25 +154,28 @@ def page_score_bound(q_rows: np.ndarray, q_scale: np.ndarray, kdeq: np.ndarray) 
     return 1e-3 * mag.max(axis=1)
 
 
-def own_page(seq_len: int, query_len: int, i: int) -> int:
-    """Own page of query i (slot 8 - query_len + i): (seq_len - query_len + i) // 128, floored."""
-    return (int(seq_len) - int(query_len) + int(i)) // PAGE_TOKENS
+def own_page(seq_len: int, query_len: int, i: int, page_tokens: int = PAGE_TOKENS) -> int:
+    """Own page of query i (slot 8 - query_len + i): (seq_len - query_len + i) // page_tokens, floored."""
+    return (int(seq_len) - int(query_len) + int(i)) // page_tokens
 
 
-def scored_pages(seq_len: int, max_blocks: int, width: int) -> int:
-    """Pages scored for a request: (seq_len - 1) // 128, clamped to [0, min(table, width)]."""
-    hist = (int(seq_len) - 1) // PAGE_TOKENS
+def scored_pages(seq_len: int, max_blocks: int, width: int, page_tokens: int = PAGE_TOKENS) -> int:
+    """Pages scored for a request: (seq_len - 1) // page_tokens, clamped to [0, min(table, width)]."""
+    hist = (int(seq_len) - 1) // page_tokens
     return max(0, min(hist, int(max_blocks), int(width)))
 
 
-def decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, pages=None):
+def decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, pages=None,
+                  page_tokens: int = PAGE_TOKENS):
     """Scores [B, 32, width] float32 of every (slot, head) row for the pages below
     the slot's own page; untouched entries stay NaN.
 
     Returns (scores, written mask, bound, status).  ``pages`` optionally
     restricts the work to a list of (b, j) pairs (sampled checks).
+    ``page_tokens`` is 128 or 256 (P256 pages).
     """
-    kv = np.asarray(kv).reshape(-1, PAGE_BYTES)
+    pt = int(page_tokens)
+    kv = np.asarray(kv).reshape(-1, page_bytes(pt))
     num_blocks = kv.shape[0]
     B = len(seq_lens)
     scores = np.full((B, ROWS, width), np.nan, dtype=np.float32)
@@ -170,18 +183,18 @@ def decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, pa
     bound = np.zeros((B, ROWS, width), dtype=np.float64)
     status = 0
     if pages is None:
-        pages = [(b, j) for b in range(B) for j in range(scored_pages(seq_lens[b], max_blocks, width))]
+        pages = [(b, j) for b in range(B) for j in range(scored_pages(seq_lens[b], max_blocks, width, pt))]
     for b in range(B):
-        if (int(seq_lens[b]) - 1) // PAGE_TOKENS > min(int(max_blocks), int(width)):
+        if (int(seq_lens[b]) - 1) // pt > min(int(max_blocks), int(width)):
             status |= ST_LEN_CLAMPED
     for b, j in pages:
-        if j >= scored_pages(seq_lens[b], max_blocks, width):
+        if j >= scored_pages(seq_lens[b], max_blocks, width, pt):
             continue
         blk = int(bt[b, j])
         q_rows = np.asarray(q[b]).reshape(ROWS, HEAD_DIM)
         qs = np.asarray(q_scale[b]).reshape(ROWS)
         if 0 <= blk < num_blocks:
-            kdeq = dequant_page(kv[blk])
+            kdeq = dequant_page(kv[blk], pt)
             s = page_scores(q_rows, qs, kdeq)
             bd = page_score_bound(q_rows, qs, kdeq)
         else:
@@ -190,7 +203,7 @@ def decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, pa
             bd = np.zeros(ROWS)
         for i in range(query_len):
             slot = SLOTS - query_len + i
-            if j < own_page(seq_lens[b], query_len, i):
+            if j < own_page(seq_lens[b], query_len, i, pt):
                 rows = slice(slot * INDEX_HEADS, (slot + 1) * INDEX_HEADS)
                 scores[b, rows, j] = s[rows]
                 written[b, rows, j] = True
@@ -283,25 +296,28 @@ def rank16(scores: np.ndarray) -> np.ndarray:
     return np.asarray(scores, dtype=np.float32).astype(np.float16).astype(np.float32)
 
 
-def decode_step(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, scores=None, rank_16bit=False):
+def decode_step(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks, scores=None, rank_16bit=False,
+                page_tokens: int = PAGE_TOKENS):
     """Indexer decode step: out [B, query_len, 4, 16] int32.
 
     ``scores`` lets a test rank a given score buffer (for instance the GPU's
     own) instead of the oracle's, which checks the selection bit for bit.
-    ``rank_16bit`` ranks the scores after ``rank16``.
+    ``rank_16bit`` ranks the scores after ``rank16``; ``page_tokens`` is 128
+    or 256 (P256 pages).
     Returns (out, scores, status).
     """
     status = 0
     if scores is None:
-        scores, _, _, status = decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks)
+        scores, _, _, status = decode_scores(q, q_scale, kv, bt, seq_lens, query_len, width, max_blocks,
+                                             page_tokens=page_tokens)
     ranked = rank16(scores) if rank_16bit else scores
     B = len(seq_lens)
     out = np.full((B, query_len, INDEX_HEADS, TOPK), -1, dtype=np.int32)
     for b in range(B):
-        n = scored_pages(seq_lens[b], max_blocks, width)
+        n = scored_pages(seq_lens[b], max_blocks, width, page_tokens)
         for i in range(query_len):
             slot = SLOTS - query_len + i
-            own = own_page(seq_lens[b], query_len, i)
+            own = own_page(seq_lens[b], query_len, i, page_tokens)
             for h in range(INDEX_HEADS):
                 out[b, i, h] = decode_row(own, ranked[b, slot * INDEX_HEADS + h], n)
     return out, scores, status

@@ -78,7 +78,7 @@ def _decode_piece(task):
     w = _W
     s, wr, bd, st = decode_scores(w["q"][b:b + 1], w["q_scale"][b:b + 1], w["kv"], w["bt"][b:b + 1],
                                   w["seq_lens"][b:b + 1], w["query_len"], w["width"], w["max_blocks"],
-                                  pages=[(0, j) for j in range(j0, j1)])
+                                  pages=[(0, j) for j in range(j0, j1)], page_tokens=w["page_tokens"])
     return b, j0, j1, s[0, :, j0:j1], wr[0, :, j0:j1], bd[0, :, j0:j1], st
 
 
@@ -91,16 +91,17 @@ def decode_scores_full(wl: dict, query_len: int = 8, piece: int = 128):
     from oracle.indexer import ROWS, scored_pages
 
     B, width, mb = len(wl["seq_lens"]), int(wl["width"]), int(wl["max_blocks"])
+    pt = int(wl.get("page_tokens", 128))
     tasks = []
     for b in range(B):
-        n = scored_pages(wl["seq_lens"][b], mb, width)
+        n = scored_pages(wl["seq_lens"][b], mb, width, pt)
         tasks += [(b, j, min(j + piece, n)) for j in range(0, n, piece)]
         if n == 0:
             tasks.append((b, 0, 0))  # the request's status bits still count
     shared = Shared({"kv": wl["kv"]})
     try:
         small = {k: wl[k] for k in ("q", "q_scale", "bt", "seq_lens")}
-        small.update(query_len=query_len, width=width, max_blocks=mb)
+        small.update(query_len=query_len, width=width, max_blocks=mb, page_tokens=pt)
         parts = _run(shared.spec, small, _decode_piece, tasks)
     finally:
         shared.close()

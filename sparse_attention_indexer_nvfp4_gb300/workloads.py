@@ -63,14 +63,16 @@ def random_scale_bytes(rng: np.random.Generator, n: int, special_frac: float = 0
     return s
 
 
-def random_nvfp4_pages(rng: np.random.Generator, num_blocks: int, special_frac: float = 0.0) -> np.ndarray:
-    """[num_blocks, 128, 72] uint8: 8192 code bytes then 1024 scale bytes per page."""
-    pages = np.empty((num_blocks, PAGE_BYTES), dtype=np.uint8)
-    pages[:, :CODE_BYTES] = rng.integers(0, 256, size=(num_blocks, CODE_BYTES), dtype=np.uint8)
-    pages[:, CODE_BYTES:] = random_scale_bytes(rng, num_blocks * (PAGE_BYTES - CODE_BYTES), special_frac).reshape(
-        num_blocks, PAGE_BYTES - CODE_BYTES
+def random_nvfp4_pages(rng: np.random.Generator, num_blocks: int, special_frac: float = 0.0,
+                       page_tokens: int = PAGE_TOKENS) -> np.ndarray:
+    """[num_blocks, T, 72] uint8 (T = page_tokens): T * 64 code bytes then T * 8 scale bytes per page."""
+    code, total = page_tokens * HEAD_DIM // 2, page_tokens * (HEAD_DIM // 2 + HEAD_DIM // 16)
+    pages = np.empty((num_blocks, total), dtype=np.uint8)
+    pages[:, :code] = rng.integers(0, 256, size=(num_blocks, code), dtype=np.uint8)
+    pages[:, code:] = random_scale_bytes(rng, num_blocks * (total - code), special_frac).reshape(
+        num_blocks, total - code
     )
-    return pages.reshape(num_blocks, PAGE_TOKENS, PAGE_BYTES // PAGE_TOKENS)
+    return pages.reshape(num_blocks, page_tokens, total // page_tokens)
 
 
 def random_e4m3(rng: np.random.Generator, shape) -> np.ndarray:
@@ -82,9 +84,9 @@ def random_uniform_f32(rng: np.random.Generator, shape, lo: float, hi: float) ->
     return rng.uniform(lo, hi, size=shape).astype(np.float32)
 
 
-def pages_for_len(seq_len: int) -> int:
+def pages_for_len(seq_len: int, page_tokens: int = PAGE_TOKENS) -> int:
     """Blocks a request of seq_len tokens occupies (the partial own page included)."""
-    return max(0, -(-int(seq_len) // PAGE_TOKENS))
+    return max(0, -(-int(seq_len) // page_tokens))
 
 
 # ---------------------------------------------------------------------------
@@ -103,24 +105,26 @@ def decode_workload(
     pool_slack: float = 0.01,
     seq_lens: np.ndarray | None = None,
     special_frac: float = 0.0,
+    page_tokens: int = PAGE_TOKENS,
 ) -> dict:
     """A batch of decode requests over one shared paged pool.
 
-    Each request owns ceil(seq_len/128) distinct blocks drawn at random from
-    the pool.  With dup_frac > 0 that fraction of a request's pages is
-    overwritten with a bitwise copy of another page of the same request, so
-    the two pages score identically and tie exactly.
+    Each request owns ceil(seq_len/page_tokens) distinct blocks drawn at
+    random from the pool (pages of 128 or 256 tokens).  With dup_frac > 0
+    that fraction of a request's pages is overwritten with a bitwise copy of
+    another page of the same request, so the two pages score identically and
+    tie exactly.
     """
     rng = rng_for(seed)
     if seq_lens is None:
         seq_lens = rng.integers(seq_lo, seq_hi + 1, size=num_reqs).astype(np.int32)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
-    need = np.array([pages_for_len(s) for s in seq_lens], dtype=np.int64)
+    need = np.array([pages_for_len(s, page_tokens) for s in seq_lens], dtype=np.int64)
     if max_blocks is None:
         max_blocks = int(max(1, need.max() if len(need) else 1))
     total = int(need.sum())
     num_blocks = max(1, int(total * (1.0 + pool_slack)) + 1)
-    kv = random_nvfp4_pages(rng, num_blocks, special_frac)
+    kv = random_nvfp4_pages(rng, num_blocks, special_frac, page_tokens)
     perm = rng.permutation(num_blocks).astype(np.int32)
     bt = np.zeros((num_reqs, max_blocks), dtype=np.int32)
     off = 0
@@ -131,7 +135,7 @@ def decode_workload(
         bt[b, n:] = perm[off] if n > 0 else 0
         off += int(need[b])
     if dup_frac > 0.0:
-        flat = kv.reshape(num_blocks, PAGE_BYTES)
+        flat = kv.reshape(num_blocks, -1)
         for b in range(num_reqs):
             n = int(min(need[b], max_blocks))
             if n < 2:
@@ -147,6 +151,7 @@ def decode_workload(
     return dict(
         kv=kv, bt=bt, seq_lens=seq_lens, q=q, q_scale=q_scale, width=int(width),
         max_blocks=int(max_blocks), query_len=int(query_len), num_blocks=int(num_blocks),
+        page_tokens=int(page_tokens),
     )
 
 
@@ -158,14 +163,17 @@ def tiny_decode(seed: int = 0) -> dict:
     q = random_e4m3(rng, (1, SLOTS, INDEX_HEADS, HEAD_DIM))
     q_scale = random_uniform_f32(rng, (1, SLOTS, INDEX_HEADS), 0.5, 2.0)
     return dict(kv=kv, bt=bt, seq_lens=np.array([4096], dtype=np.int32), q=q, q_scale=q_scale,
-                width=32, max_blocks=32, query_len=SLOTS, num_blocks=32)
+                width=32, max_blocks=32, query_len=SLOTS, num_blocks=32, page_tokens=PAGE_TOKENS)
 
 
 def batched_decode(seed: int = 2, num_reqs: int = 64, seq_lo: int = 8192, seq_hi: int = 172032,
-                   width: int = 1344, dup_frac: float = 0.01) -> dict:
-    """64 requests, seq_len U[8K, 168K], 1% duplicated pages, 1,344-column rows."""
-    return decode_workload(seed, num_reqs, seq_lo, seq_hi, width, max_blocks=-(-seq_hi // PAGE_TOKENS),
-                           dup_frac=dup_frac)
+                   width: int | None = None, dup_frac: float = 0.01, page_tokens: int = PAGE_TOKENS) -> dict:
+    """64 requests, seq_len U[8K, 168K], 1% duplicated pages; 1,344-column rows
+    with P128 pages, 672 with P256."""
+    if width is None:
+        width = 172032 // page_tokens
+    return decode_workload(seed, num_reqs, seq_lo, seq_hi, width, max_blocks=-(-seq_hi // page_tokens),
+                           dup_frac=dup_frac, page_tokens=page_tokens)
 
 
 def long_context(seed: int = 4, num_reqs: int = 16, seq_len: int = 500_000) -> dict:
