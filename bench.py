@@ -551,6 +551,28 @@ def secondary(args, torch, idx, W, timer, hbm_peak, main) -> dict:
                               "ms_step": step1, "ms_scorer": score, "scores_per_s": u1["scores"] / (step1 / 1e3),
                               "index_k_gbs": u1["pages"] * PAGE_BYTES / (score / 1e3) / 1e9}
 
+    if "p256" in args.legs:
+        # the batched decode on P256 pages: 672-column rows, each page scored as two 128-key halves
+        wl = W.batched_decode(page_tokens=256)
+        q, qs, kv, bt, sl = (to_dev(wl[k]) for k in ("q", "q_scale", "kv", "bt", "seq_lens"))
+        B = len(wl["seq_lens"])
+        sc = torch.empty((B, 32, 2 * wl["width"]), dtype=torch.float32, device="cuda")
+        out = torch.empty((B, 8, 4, 16), dtype=torch.int32, device="cuda")
+        wsb = idx.idx_decode_workspace_bytes(B, 8, wl["width"])
+        ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
+        fn = lambda: idx.idx_decode_step(q, qs, kv, bt, sl, 8, sc, out, ws, flags=idx.PAGE_256)
+        fn()
+        ms = timer.run(fn, iters)
+        units = sum(2 * max(0, min((int(s) - 1) // 256, wl["width"])) for s in wl["seq_lens"])
+        pages = units // 2
+        byts = units * PAGE_BYTES
+        res["p256"] = {"workload": "batched decode on P256 pages: 64 requests, seq_len U[8K,168K], 672-column rows",
+                       "ms": ms, "pages_per_step": pages, "scores_per_s": pages * 32 / (ms / 1e3),
+                       "index_k_gbs": byts / (ms / 1e3) / 1e9, "frac_of_hbm": byts / (ms / 1e3) / 1e9 / hbm_peak,
+                       "launches": 2 + (1 if wsb else 0)}
+        del q, qs, kv, bt, sl, sc, out, ws, wl
+        torch.cuda.empty_cache()
+
     if "sweep" in args.legs:
         # standalone top-16: 4,096 rows per width, 1% specials and ties, ragged valid counts
         out = torch.empty((4096, 16), dtype=torch.int32, device="cuda")
@@ -677,8 +699,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip secondary workloads; short CPU baseline")
-    ap.add_argument("--legs", default="gather,long,mtp,prefill,tiny,qlen1,sweep,mxfp8",
-                    help="secondary workloads to time (comma list of gather, long, mtp, prefill, tiny, qlen1, sweep, mxfp8; "
+    ap.add_argument("--legs", default="gather,long,mtp,prefill,p256,tiny,qlen1,sweep,mxfp8",
+                    help="secondary workloads to time (comma list of gather, long, mtp, prefill, p256, tiny, qlen1, sweep, mxfp8; "
                          "empty for none)")
     args = ap.parse_args()
     args.legs = set() if args.quick else {x for x in args.legs.split(",") if x}

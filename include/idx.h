@@ -216,12 +216,26 @@ int idx_topk16_select_noalloc(const float* scores, int64_t row_stride, int32_t r
  *   workspace     >= idx_decode_workspace_bytes(num_reqs, query_len, width)
  *                 bytes, 8-byte aligned; its contents need no initialisation
  *                 (NULL when that is 0).
- *   flags         0, or IDX_RANK_16BIT: rank the scores rounded to IEEE
+ *   flags         IDX_RANK_16BIT: rank the scores rounded to IEEE
  *                 binary16 (round to nearest even, overflow to infinity),
  *                 as the stock decode ranks 16-bit quantized scores ([CP]
  *                 module docstring); scores equal in 16 bits then rank by
  *                 page (lower first).  The score buffer keeps the fp32
- *                 scores.  Other bits: IDX_E_BAD_SHAPE.
+ *                 scores.
+ *                 IDX_PAGE_256: P256 pages ([PUBLISH] Performance: P128
+ *                 and P256 pages, 672 columns at 168K tokens).  kv is
+ *                 [num_blocks, 256, 72]: 18,432 bytes a page, token t's 64
+ *                 code bytes at t*64, then its 8 scale bytes at
+ *                 16,384 + t*8; block ids, max_blocks and width count
+ *                 256-token pages; a query's own page is
+ *                 floor((seq_len - query_len + i) / 256) and pages below
+ *                 (seq_len-1)/256 are scored; a page's score is the max over
+ *                 its 256 keys.  scores_ws is then [num_reqs, 32, 2*width],
+ *                 8-byte aligned: column 2j+h holds the max over keys
+ *                 [128h, 128h+128) of page j (stored where page j is, i.e.
+ *                 below the own page), and the page's score is the larger
+ *                 of the pair.
+ *                 Other bits: IDX_E_BAD_SHAPE.
  * Other arguments as in idx_score_pages.
  *
  * idx_decode_workspace_bytes: the selector's workspace for the step's
@@ -230,6 +244,7 @@ int idx_topk16_select_noalloc(const float* scores, int64_t row_stride, int32_t r
  */
 size_t idx_decode_workspace_bytes(int32_t num_reqs, int32_t query_len, int32_t width);
 #define IDX_RANK_16BIT 1
+#define IDX_PAGE_256 2
 int idx_decode_step(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
                     const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                     const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,

@@ -203,10 +203,11 @@ class DecodeSampler:
 
         self.piece = piece
         self.cores = processes or cores()
-        self.n = [scored_pages(s, wl["max_blocks"], wl["width"]) for s in wl["seq_lens"]]
+        pt = int(wl.get("page_tokens", 128))
+        self.n = [scored_pages(s, wl["max_blocks"], wl["width"], pt) for s in wl["seq_lens"]]
         self.shared = Shared({"kv": wl["kv"]})
         small = {k: wl[k] for k in ("q", "q_scale", "bt", "seq_lens")}
-        small.update(query_len=query_len, width=int(wl["width"]), max_blocks=int(wl["max_blocks"]))
+        small.update(query_len=query_len, width=int(wl["width"]), max_blocks=int(wl["max_blocks"]), page_tokens=pt)
         self.pool = mp.get_context("spawn").Pool(processes=self.cores, initializer=_init,
                                                  initargs=(self.shared.spec, small))
         first = next(b for b, n in enumerate(self.n) if n > 0)

@@ -30,6 +30,7 @@ __all__ = [
     "NOALLOC_SCRATCH_BYTES",
     "idx_decode_step",
     "RANK_16BIT",
+    "PAGE_256",
     "idx_mtp_score_fp8",
     "idx_prefill_workspace_bytes",
     "idx_prefill_index_step",
@@ -210,16 +211,19 @@ def idx_topk16_select_noalloc(scores, out_idx, valid_n=None, force_begin: int = 
 
 
 RANK_16BIT = 1  # idx_decode_step flag: rank the scores rounded to binary16
+PAGE_256 = 2  # idx_decode_step flag: P256 pages (scores_ws [B, 32, 2 * width], a page the max of a column pair)
 
 
 def idx_decode_step(q, q_scale, kv, block_table, seq_lens, query_len: int, scores_ws, out, workspace=None,
                     status=None, stream=None, flags: int = 0) -> int:
-    """One decode step: scores into scores_ws [B,32,width], rows into out [B,query_len,4,16] i32."""
+    """One decode step: scores into scores_ws [B,32,width] ([B,32,2*width] with PAGE_256), rows into
+    out [B,query_len,4,16] i32."""
     lib = load_library()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    width = scores_ws.shape[-1] // (2 if flags & PAGE_256 else 1)
     return _check("idx_decode_step", lib.idx_decode_step(
         _ptr(q), _ptr(q_scale), _ptr(kv), kv.shape[0], _ptr(block_table), _row_stride(block_table),
-        block_table.shape[1], _ptr(seq_lens), seq_lens.shape[0], int(query_len), scores_ws.shape[-1],
+        block_table.shape[1], _ptr(seq_lens), seq_lens.shape[0], int(query_len), width,
         _ptr(scores_ws), _ptr(out), _ptr(workspace), ws_bytes, int(flags), _ptr(status), _stream(stream)))
 
 

@@ -13,7 +13,8 @@ namespace idx {
 
 int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
-                    int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream);
+                    int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream,
+                    int32_t page_tokens);
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -77,9 +78,9 @@ int launch_result() {
 int launch_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
                        const int32_t* bt, int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens,
                        int32_t num_reqs, int32_t query_len, int32_t width, float* scores, int32_t* status,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, int32_t page_tokens) {
   return launch_score_tc(q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks, seq_lens, num_reqs, query_len, width,
-                         scores, status, stream);
+                         scores, status, stream, page_tokens);
 }
 
 namespace {
@@ -133,7 +134,7 @@ extern "C" int idx_score_pages(const uint8_t* q, const float* q_scale, const uin
   if (rc != IDX_OK) return rc;
   if ((rc = check_device()) != IDX_OK) return rc;
   return launch_score_pages(q, q_scale, kv, num_blocks, block_table, bt_stride, max_blocks, seq_lens, num_reqs,
-                            query_len, width, scores, status, (cudaStream_t)stream);
+                            query_len, width, scores, status, (cudaStream_t)stream, kPageTokens);
 }
 
 extern "C" size_t idx_decode_workspace_bytes(int32_t num_reqs, int32_t query_len, int32_t width) {
@@ -148,10 +149,13 @@ extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uin
                                int32_t flags, int32_t* status, void* stream) {
   using namespace idx;
   if (num_reqs < 0 || width < 0 || max_blocks < 0 || query_len < 1 || query_len > kSlots) return IDX_E_BAD_SHAPE;
-  if ((flags & ~IDX_RANK_16BIT) != 0) return IDX_E_BAD_SHAPE;
+  if ((flags & ~(IDX_RANK_16BIT | IDX_PAGE_256)) != 0) return IDX_E_BAD_SHAPE;
   if (num_reqs == 0) return IDX_OK;
   if (!out || !seq_lens) return IDX_E_NULL_PTR;
-  if (!aligned(out, 4) || !aligned(workspace, 8)) return IDX_E_MISALIGNED;
+  const int32_t page_tokens = (flags & IDX_PAGE_256) ? 2 * kPageTokens : kPageTokens;
+  // P256: the selector reads a row's two 128-key columns of a page as one 8-byte load
+  if (!aligned(out, 4) || !aligned(workspace, 8) || ((flags & IDX_PAGE_256) && !aligned(scores_ws, 8)))
+    return IDX_E_MISALIGNED;
   int rc;
   const bool any_pages = width > 0 && max_blocks > 0;
   if (any_pages) {
@@ -165,10 +169,10 @@ extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uin
   cudaStream_t s = (cudaStream_t)stream;
   if (any_pages) {
     rc = launch_score_pages(q, q_scale, kv, num_blocks, block_table, bt_stride, max_blocks, seq_lens, num_reqs,
-                            query_len, width, scores_ws, status, s);
+                            query_len, width, scores_ws, status, s, page_tokens);
     if (rc != IDX_OK) return rc;
   }
   DecodeRows d{scores_ws, seq_lens, num_reqs, query_len, width, any_pages ? max_blocks : 0, out,
-               (flags & IDX_RANK_16BIT) != 0};
+               (flags & IDX_RANK_16BIT) != 0, page_tokens};
   return launch_topk_decode(d, workspace, s);
 }

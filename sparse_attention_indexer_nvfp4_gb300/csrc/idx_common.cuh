@@ -39,6 +39,8 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 
 // floor((a) / 128) for possibly negative a
 __device__ __forceinline__ int floor_div_page(int a) { return a >= 0 ? a / kPageTokens : -((-a + kPageTokens - 1) / kPageTokens); }
+// floor(a / d) for d > 0
+__device__ __forceinline__ int floor_div(int a, int d) { return a >= 0 ? a / d : -((-a + d - 1) / d); }
 
 // ---------------------------------------------------------------------------
 // E4M3 / E2M1 conversions

@@ -101,12 +101,15 @@ struct DecodeRows {
   int32_t num_reqs, query_len, width, max_blocks;
   int32_t* out;  // [B, query_len, 4, 16]
   bool rank16;   // rank the scores rounded to binary16 (IDX_RANK_16BIT)
+  int32_t page_tokens;  // 128, or 256 (IDX_PAGE_256: rows of 2 * width columns, a page the max of a pair)
 };
 
+// page_tokens 128 or 256; with 256 each (slot, head) row has 2 * width
+// columns, column 2j + h the max over keys [128h, 128h + 128) of page j.
 int launch_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
                        const int32_t* bt, int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens,
                        int32_t num_reqs, int32_t query_len, int32_t width, float* scores, int32_t* status,
-                       cudaStream_t stream);
+                       cudaStream_t stream, int32_t page_tokens);
 
 
 

@@ -194,7 +194,23 @@ struct Misc {
   int stored[kPipe];  // last page issuer e has stored (-1 before the first)
 };
 
-__device__ __forceinline__ int pages_of(int seq, int cap) { return max(0, min(floor_div_page(seq - 1), cap)); }
+// Page geometry: P128 pages (128 keys, 9,216 bytes) or P256 pages (256 keys,
+// 18,432 bytes: the 16,384 code bytes of all 256 tokens, then their 2,048
+// scale bytes).  The pipeline always works on 128-key units: a P256 page is
+// two units (half h: tokens [128h, 128h + 128), its codes at h * 8,192 and
+// its scales at 16,384 + h * 1,024), each scored into its own column 2j + h
+// of a row twice as wide; the selector takes the max of the pair.
+template <bool kP256>
+struct Geo {
+  static constexpr int kTokens = kP256 ? 2 * kPageTokens : kPageTokens;
+  static constexpr int kUnits = kP256 ? 2 : 1;  // 128-key units per page
+};
+
+// 128-key units scored for a request: pages below its last, clamped to cap pages
+template <bool kP256>
+__device__ __forceinline__ int units_of(int seq, int cap) {
+  return Geo<kP256>::kUnits * max(0, min(floor_div(seq - 1, Geo<kP256>::kTokens), cap));
+}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
@@ -261,6 +277,7 @@ __device__ __forceinline__ int ld_acquire_shared(const int* p) {
   return v;
 }
 
+template <bool kP256>
 __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     const uint8_t* __restrict__ q, const float* __restrict__ q_scale, const uint8_t* __restrict__ kv,
     int64_t num_blocks, const int32_t* __restrict__ bt, int64_t bt_stride, int32_t max_blocks,
@@ -293,18 +310,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     bool clamped = false;
     for (int b = tid; b < num_reqs; b += kThreads) {
       const int seq = seq_lens[b];
-      const int n = pages_of(seq, cap);
+      const int n = units_of<kP256>(seq, cap);
       if (b < kReqCache) req_pages[b] = n;  // the slice search and the page records read these
       local += (unsigned long long)n;
-      clamped |= floor_div_page(seq - 1) > cap;
+      clamped |= floor_div(seq - 1, Geo<kP256>::kTokens) > cap;
     }
     if (clamped && blockIdx.x == 0) report(status, IDX_ST_LEN_CLAMPED);
     local = warp_sum_u64(local);
     if ((tid & 31) == 0 && local) atomicAdd(&misc->total, local);
   }
   __syncthreads();
-  // pages of request b (shared memory for the first kReqCache requests)
-  auto npages = [&](int b) -> int { return b < kReqCache ? req_pages[b] : pages_of(seq_lens[b], cap); };
+  // units of request b (shared memory for the first kReqCache requests)
+  auto npages = [&](int b) -> int { return b < kReqCache ? req_pages[b] : units_of<kP256>(seq_lens[b], cap); };
   const unsigned long long P = misc->total;
   const unsigned long long p0 = P * blockIdx.x / gridDim.x, p1 = P * (blockIdx.x + 1) / gridDim.x;
   const int count = (int)(p1 - p0);
@@ -407,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
           n3 = b3 < num_reqs ? npages(b3) : 0;
         }
         const bool live = p < count;
-        const int blk = live ? bt[(int64_t)b * bt_stride + j] : -1;
+        const int blk = live ? bt[(int64_t)b * bt_stride + (kP256 ? j >> 1 : j)] : -1;
         const int nq = (live && p + kPipe < count && b3 != b) ? b3 : -1;
         // whether each request of the chunk has a q_scale that is not >= 0
         // (the epilogue then reduces with min too)
@@ -435,8 +452,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
         const int blk = recs[i % kRecs].blk;
         if (blk >= 0 && blk < num_blocks) {
           mbar_arrive_expect_tx(&bars[kRawFull + lane], kPageBytes);
-          bulk_g2s(smem + kOffRaw + lane * kPageBytes, kv + (int64_t)blk * kPageBytes, kPageBytes,
-                   &bars[kRawFull + lane]);
+          if (kP256) {
+            // the unit's codes and scales, laid out in the stage as a P128 page
+            const int h = recs[i % kRecs].j & 1;
+            const uint8_t* src = kv + (int64_t)blk * (2 * kPageBytes);
+            bulk_g2s(smem + kOffRaw + lane * kPageBytes, src + h * kCodeBytes, kCodeBytes, &bars[kRawFull + lane]);
+            bulk_g2s(smem + kOffRaw + lane * kPageBytes + kCodeBytes,
+                     src + 2 * kCodeBytes + h * (kPageBytes - kCodeBytes), kPageBytes - kCodeBytes,
+                     &bars[kRawFull + lane]);
+          } else {
+            bulk_g2s(smem + kOffRaw + lane * kPageBytes, kv + (int64_t)blk * kPageBytes, kPageBytes,
+                     &bars[kRawFull + lane]);
+          }
         } else {
           mbar_arrive(&bars[kRawFull + lane]);
         }
@@ -490,11 +517,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       if (r.b != prev_b) {
         prev_b = r.b;
         qs = q_scale[(int64_t)prev_b * kRows + lane];
-        own = iq >= 0 ? floor_div_page(seq_lens[prev_b] - query_len + iq) : -1;
+        // in units: the units of the pages below the slot's own page
+        own = iq >= 0 ? Geo<kP256>::kUnits * floor_div(seq_lens[prev_b] - query_len + iq, Geo<kP256>::kTokens) : -1;
       }
       float val = qs >= 0.f ? qs * mx : qs * mn;
       if (!(r.blk >= 0 && r.blk < num_blocks)) val = __int_as_float(0x7FC00000);  // NaN: ranked as -inf
-      if (r.j < own) scores[((int64_t)r.b * kRows + lane) * width + r.j] = val;
+      if (r.j < own) scores[((int64_t)r.b * kRows + lane) * (int64_t)(Geo<kP256>::kUnits * width) + r.j] = val;
     };
     bool issued_any = false, ok = true;
     int last = -1;  // the last page issued
@@ -684,27 +712,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
 int g_sms[64];
 bool g_attr[64];
 
+template <bool kP256>
+bool set_attrs() {
+  return cudaFuncSetAttribute(k_score_decode<kP256>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ==
+             cudaSuccess &&
+         cudaFuncSetAttribute(k_score_decode<kP256>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+}
+
 }  // namespace
 
 int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
-                    int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream) {
+                    int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream,
+                    int32_t page_tokens) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IDX_E_CUDA;
   if (!g_attr[dev]) {
-    if (cudaFuncSetAttribute(k_score_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(k_score_decode, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-      return IDX_E_CUDA;
+    if (!set_attrs<false>() || !set_attrs<true>()) return IDX_E_CUDA;
     if (cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return IDX_E_CUDA;
     g_attr[dev] = true;
   }
-  const int64_t upper = (int64_t)num_reqs * (int64_t)min(width, max_blocks);
+  const bool p256 = page_tokens == 2 * kPageTokens;
+  const int64_t upper = (int64_t)num_reqs * (int64_t)min(width, max_blocks) * (p256 ? 2 : 1);
   if (upper <= 0) return IDX_OK;
+  if (upper > 0x7FFFFFFFLL) return IDX_E_TOO_LARGE;
   // one CTA per SM: each CTA holds all 512 TMEM columns of its SM
   const int grid = (int)std::min<int64_t>((int64_t)g_sms[dev], upper);
-  launch_pdl(k_score_decode, dim3(grid), dim3(kThreads), kSmemBytes, stream, q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks,
-                                                          seq_lens, num_reqs, query_len, width, scores, status, wait_polls());
+  launch_pdl(p256 ? k_score_decode<true> : k_score_decode<false>, dim3(grid), dim3(kThreads), kSmemBytes, stream, q,
+             q_scale, kv, num_blocks, bt, bt_stride, max_blocks, seq_lens, num_reqs, query_len, width, scores, status,
+             wait_polls());
   return launch_result();
 }
 

@@ -163,10 +163,12 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
 // result, descending, 0 padding.
 // With rank16 every score is first rounded to binary16 (round to nearest
 // even, overflow to infinity) and widened back, so scores that tie in 16
-// bits rank by column.
+// bits rank by column.  With pair, column c's score is the max of row[2c]
+// and row[2c + 1] (a P256 page scored as two 128-key halves; row 8-byte
+// aligned).
 template <int K, bool kForce>
 __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
-                                   bool rank16 = false) {
+                                   bool rank16 = false, bool pair = false) {
   const uint32_t lane = lane_id();
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int nch = (c1 - c0 + 31) >> 5;
@@ -176,7 +178,13 @@ __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1
     const int col = c0 + i * 32 + (int)lane;
     uint32_t v = 0;
     if (i < nch && col < c1) {
-      float x = __ldg(row + col);
+      float x;
+      if (pair) {
+        const float2 h = __ldg(reinterpret_cast<const float2*>(row) + col);
+        x = fmaxf(h.x, h.y);
+      } else {
+        x = __ldg(row + col);
+      }
       if (rank16) x = __half2float(__float2half_rn(x));
       v = ordered_bits(x);
       if (kForce && col >= fb && col < fe) v = kOrderedPosInf;

@@ -78,11 +78,12 @@ __device__ __forceinline__ DecodeRowInfo decode_info(const DecodeRows& d, int64_
   const int seq = d.seq_lens[b];
   const int slot = kSlots - d.query_len + i;
   DecodeRowInfo info;
-  info.own = floor_div_page(seq - d.query_len + i);
-  const int hist = floor_div_page(seq - 1);
+  info.own = floor_div(seq - d.query_len + i, d.page_tokens);
+  const int hist = floor_div(seq - 1, d.page_tokens);
   const int scored = max(0, min(hist, min(d.max_blocks, d.width)));
   info.n = max(0, min(info.own, scored));
-  info.row = d.scores + ((int64_t)b * kRows + slot * kHeads + h) * d.width;
+  const int64_t stride = (int64_t)d.width * (d.page_tokens / kPageTokens);  // P256: two columns a page
+  info.row = d.scores + ((int64_t)b * kRows + slot * kHeads + h) * stride;
   return info;
 }
 
@@ -134,7 +135,9 @@ __global__ void __launch_bounds__(128) k_topk_rows(PlainRows p, DecodeRows d, in
   const int c0 = kWarps == 1 ? 0 : (split * kWarps + (int)warp) * kSeg;
   const int c1 = min(c0 + kSeg, n);
   uint64_t run = 0;
-  if (c0 < c1) run = warp_top16_seg<K, !kDecode>(row, c0, c1, fb, fe, &scratch[warp], kDecode && d.rank16);
+  if (c0 < c1)
+    run = warp_top16_seg<K, !kDecode>(row, c0, c1, fb, fe, &scratch[warp], kDecode && d.rank16,
+                                      kDecode && d.page_tokens != kPageTokens);
   run = cta_merge<kWarps>(run, cand, &scratch[0]);
   if (kWarps > 1 && warp != 0) return;
   if (nsplit == 1) {

@@ -65,7 +65,7 @@ def test_error_codes_and_strings(built):
     assert lib.idx_topk16_select(16, 100, 0, 100, None, 0, 0, None, None, None, 0, None) == 0
     assert lib.idx_mtp_score_fp8(16, 16, 4, 0, 16, 16, 8, 16, 4, 4, 16, 16, 2, 10, 16, None, None) == E_SHAPE
     assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 9000, 16, 16, None, 0, 0, None, None) == E_WS
-    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 2, None, None) == E_SHAPE  # flags
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 4, None, None) == E_SHAPE  # flags
 
 
 def test_wait_limit_setter_returns_the_previous_budget(built):
@@ -131,3 +131,12 @@ def test_prefill_workspace_sizing_and_checks(built):
         bad = list(args)
         bad[i] = v
         assert lib.idx_prefill_index_step(*bad) == want, (i, v)
+
+
+def test_decode_step_flags(built):
+    lib = built.load_library()
+    E_SHAPE, E_MIS = -2, -3
+    # P256 (flag 2) is accepted; with it the score buffer must be 8-byte aligned
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 20, 16, None, 0, 2, None, None) == E_MIS
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 4, None, None) == E_SHAPE
+    assert built.PAGE_256 == 2 and built.RANK_16BIT == 1
