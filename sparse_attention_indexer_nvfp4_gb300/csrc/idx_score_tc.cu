@@ -27,8 +27,7 @@
 //                       K-major E4M3 tile, one thread per 32 elements (two scale
 //                       groups of one key) through a per-scale lookup table
 //                       (built on the device by the exact fp32 round-once rule,
-//                       so it is the same function; 8 copies to spread a
-//                       half-warp's reads over the banks), 9 operations per 8
+//                       so it is the same function), 9 operations per 8
 //                       elements.  Each group has one warp on each of the SM's
 //                       four sub-partitions, so the integer work is spread
 //                       evenly over them;
@@ -129,7 +128,18 @@ static_assert(kQCol0 + kPipe * kQCols <= kTmemCols, "accumulators and query tile
 
 constexpr int kKTile = kPageTokens * kHeadDim;  // 16384
 constexpr int kQBytes = kRows * kHeadDim;       // 4096: one request's 32 query rows
-constexpr int kLutCopies = 8;  // lane & 7 picks a copy
+// Dequant table: one 8-byte row per scale magnitude (the scale byte's low 7
+// bits; 128 rows), 16 copies, lane & 15 picks one.  A row's copies fill one
+// 128-byte bank line, so the 16 lanes of a half-warp read 16 different bank
+// pairs whatever their scales: every 64-bit table load is two conflict-free
+// wavefronts.  (Eight copies of 256 rows put a row's copies in one half of
+// the banks, chosen by the scale's parity, and conflicted on about half the
+// loads.)  A scale with the sign bit set scales every element by -|s|:
+// e4m3_rn_satfinite is odd (RN and saturation are symmetric, and a zero code
+// gives a zero with the product's sign), so its row is the |s| row with every
+// sign flipped, which the dequant applies by flipping the codes' sign bits.
+constexpr int kLutRows = 128;
+constexpr int kLutCopies = 16;
 // Page records, written by the producer 32 at a time, read by the producer
 // (block id), the dequant group (validity), the epilogue (flags) and the
 // issuer that stores the page's scores (request, page, validity), which is
@@ -164,7 +174,7 @@ constexpr int kReqCache = 256;  // page counts of the first kReqCache requests, 
 constexpr int kOffK = 0;
 constexpr int kOffRaw = kOffK + kKTiles * kKTile;
 constexpr int kOffLut = kOffRaw + kStages * kPageBytes;
-constexpr int kOffRec = kOffLut + 256 * 8 * kLutCopies;
+constexpr int kOffRec = kOffLut + kLutRows * 8 * kLutCopies;
 constexpr int kOffScore = kOffRec + kRecs * (int)sizeof(PageRec);
 constexpr int kOffBar = kOffScore + kScoreSlots * 2 * kRows * 4;
 // K-tile full barriers are kept per (tile, issuer): pages of one tile are 8
@@ -367,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&misc->tmem_base, kTmemCols);
-  if (tid < 256) {
-    // table row of scale byte s: e4m3_rn_satfinite(m * e4m3(s)) for the magnitudes m of codes 0..7
+  if (tid < kLutRows) {
+    // table row of scale magnitude s: e4m3_rn_satfinite(m * e4m3(s)) for the magnitudes m of codes 0..7
     const uint2 row = dequant8_fp32(0x76543210u, e4m3_to_f32((uint32_t)tid));
 #pragma unroll
     for (int c = 0; c < kLutCopies; ++c) lut[tid * kLutCopies + c] = row;
@@ -647,6 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     const int c = lane & 3, t0 = wg * 32 + (lane >> 2);
     const uint32_t swz0 = (uint32_t)(((2 * c) ^ (t0 & 7)) << 4), swz1 = (uint32_t)(((2 * c + 1) ^ (t0 & 7)) << 4);
     const uint2* lut_l = lut + (lane & (kLutCopies - 1));
+    static_assert(kLutCopies * 8 == 128, "a row's copies fill one bank line");
     for (int i = grp; i < count; i += kGroups) {
       const int stage = i % kStages;
       const int tile = grp * kGroupTiles + (i / kGroups) % kGroupTiles;  // used by pages i, i + 8, ... of this group
@@ -683,11 +694,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       const uint32_t loaded = __ballot_sync(0xFFFFFFFFu, dep == 0u);
       if (lane == 0) mbar_arrive_after(&bars[kRawEmpty + stage], loaded);
       if (page_valid) {
+        // scales with the sign bit set (rare; none in ordinary caches): flip
+        // the sign bits of the codes they scale, then look up |s|
+        if (__any_sync(0xFFFFFFFFu, ((sc[0] | sc[1] | sc[2] | sc[3]) & 0x8080u) != 0u)) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t f0 = (sc[k] & 0x80u) ? 0x88888888u : 0u, f1 = (sc[k] & 0x8000u) ? 0x88888888u : 0u;
+            cw[k].x ^= f0, cw[k].y ^= f0, cw[k].z ^= f1, cw[k].w ^= f1;
+          }
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int t = t0 + 8 * k;
-          const uint2 L0 = lut_l[(sc[k] & 0xFFu) * kLutCopies];
-          const uint2 L1 = lut_l[(sc[k] >> 8) * kLutCopies];
+          const uint2 L0 = lut_l[(sc[k] & 0x7Fu) * kLutCopies];
+          const uint2 L1 = lut_l[((sc[k] >> 8) & 0x7Fu) * kLutCopies];
           const uint2 a = dq8_lut(cw[k].x, L0.x, L0.y), bb = dq8_lut(cw[k].y, L0.x, L0.y);
           const uint2 e2 = dq8_lut(cw[k].z, L1.x, L1.y), f = dq8_lut(cw[k].w, L1.x, L1.y);
           *reinterpret_cast<uint4*>(kd + t * kHeadDim + swz0) = make_uint4(a.x, a.y, bb.x, bb.y);
