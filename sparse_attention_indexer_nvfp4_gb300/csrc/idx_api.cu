@@ -59,7 +59,19 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t ra
 
 namespace {
 std::atomic<uint32_t> g_wait_polls{kWaitPolls};
+std::atomic<int> g_dev_sms[kMaxDevices];
 }  // namespace
+
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = g_dev_sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 0) return 0;
+    g_dev_sms[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 
 uint32_t wait_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
 
