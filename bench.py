@@ -525,6 +525,24 @@ def secondary(args, torch, idx, W, timer, hbm_peak, main) -> dict:
     def to_dev(x):
         return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
+    fp8_peak = None
+    if "fp8" in args.legs:
+        # dense FP8 tensor-core rate (tcgen05.mma kind::f8f6f4, M=128 x N=256 x K=32, one CTA per SM), the
+        # denominator of the multi-token and prefill scorers' tensor figures; median of 5 launches of ~3 ms
+        chk = torch.zeros(1, dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        n_it = 10000
+        flops = idx.idx_fp8_mma_probe(n_it, chk, st)
+        torch.cuda.synchronize()
+        assert float(chk.item()) == 32.0 * n_it and int(st.item()) == 0
+        vals = [timer.run(lambda: idx.idx_fp8_mma_probe(n_it, None, st), 1) for _ in range(5)]
+        fp8_peak = flops / (statistics.median(vals) / 1e3) / 1e12
+        res["fp8_dense_peak"] = {"tflops": fp8_peak, "ms_per_launch": statistics.median(vals),
+                                 "method": "idx_fp8_mma_probe: one CTA per SM issues 4 x 10,000 tcgen05.mma "
+                                           "kind::f8f6f4 M=128 x N=256 x K=32 (E4M3, fp32 accumulation in TMEM) "
+                                           "back to back; CUDA events, median of 5 launches",
+                                 "frac_of_nominal_4500": fp8_peak / 4500.0}
+
     if "tiny" in args.legs:
         # tiny decode: 1 request x 4,096 tokens, 31 pages scored
         t = W.tiny_decode(0)
@@ -667,6 +685,8 @@ def secondary(args, torch, idx, W, timer, hbm_peak, main) -> dict:
                       "token_keys_per_s": T * m["max_keys"] / (ms / 1e3),
                       "scorer_tflops": flops / (ms_s / 1e3) / 1e12, "scorer_gbs": kbytes / (ms_s / 1e3) / 1e9,
                       "scorer_frac_of_hbm": kbytes / (ms_s / 1e3) / 1e9 / hbm_peak, "launches": 2 + (1 if wsb else 0)}
+        if fp8_peak:
+            res["mtp"]["scorer_frac_of_fp8_peak"] = flops / (ms_s / 1e3) / 1e12 / fp8_peak
 
     if "prefill" in args.legs:
         # Q8KV8 prefill chain: gather-dequant, causal relu-weighted scores, top-16 per token
@@ -686,6 +706,8 @@ def secondary(args, torch, idx, W, timer, hbm_peak, main) -> dict:
                                       "top-16 per token", "ms": ms, "token_keys_per_s": tok_keys / (ms / 1e3),
                           "tflops": flops / (ms / 1e3) / 1e12, "launches": 4 + (1 if idx.idx_workspace_bytes(T, mk)
                                                                                  else 0)}
+        if fp8_peak:
+            res["prefill"]["frac_of_fp8_peak"] = flops / (ms / 1e3) / 1e12 / fp8_peak
         del kv, bt, nk, cu, q, qs, sc, out, ws
         torch.cuda.empty_cache()
 
@@ -699,9 +721,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip secondary workloads; short CPU baseline")
-    ap.add_argument("--legs", default="gather,long,mtp,prefill,p256,tiny,qlen1,sweep,mxfp8",
-                    help="secondary workloads to time (comma list of gather, long, mtp, prefill, p256, tiny, qlen1, sweep, mxfp8; "
-                         "empty for none)")
+    ap.add_argument("--legs", default="fp8,gather,long,mtp,prefill,p256,tiny,qlen1,sweep,mxfp8",
+                    help="secondary workloads to time (comma list of fp8, gather, long, mtp, prefill, p256, tiny, qlen1, "
+                         "sweep, mxfp8; empty for none)")
     args = ap.parse_args()
     args.legs = set() if args.quick else {x for x in args.legs.split(",") if x}
 

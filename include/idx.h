@@ -349,6 +349,24 @@ int idx_prefill_index_step(const uint8_t* kv, int64_t num_blocks, const int32_t*
 int idx_mxfp8_quantize(const uint16_t* x_bf16, int64_t rows, int64_t cols, int64_t x_stride, uint8_t* out_e4m3,
                        int64_t out_stride, uint8_t* scales_e8m0, int64_t scale_stride, void* stream);
 
+/*
+ * Dense FP8 tensor-core throughput probe.  Not a step of the indexer: the
+ * pages state no tensor-core rate, and this call measures the one the
+ * multi-token and prefill scorers (tcgen05.mma kind::f8f6f4) are compared
+ * against.  One CTA per SM issues `iters` rounds of four M=128 x N=256 x K=32
+ * E4M3 MMAs (fp32 accumulation in tensor memory) back to back; time the
+ * launch with events on `stream`.
+ *
+ *   iters    1 .. 100,000 (IDX_E_BAD_SHAPE otherwise).
+ *   check    optional (may be NULL) float in device memory, 4-byte aligned:
+ *            receives accumulator element (0, 0) of the first CTA, which is
+ *            32 * iters exactly (every operand element is 0.5).
+ *   flops    optional host pointer: receives the launch's floating-point
+ *            operations, 2 * 128 * 256 * 32 * 4 * iters * SMs.
+ *   status   optional; IDX_ST_TIMEOUT if the final wait gave up.
+ */
+int idx_fp8_mma_probe(int32_t iters, float* check, double* flops, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

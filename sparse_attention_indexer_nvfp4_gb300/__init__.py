@@ -35,6 +35,7 @@ __all__ = [
     "idx_prefill_workspace_bytes",
     "idx_prefill_index_step",
     "idx_mxfp8_quantize",
+    "idx_fp8_mma_probe",
     "SYMBOLS",
     "ST_BLOCK_OOR",
     "ST_LEN_CLAMPED",
@@ -76,6 +77,7 @@ SYMBOLS = {
     "idx_prefill_index_step": (ctypes.c_int, [_p, _i64, _p, _i64, _i32, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _p, _p,
                                               _p, _sz, _p, _p]),
     "idx_mxfp8_quantize": (ctypes.c_int, [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, _p]),
+    "idx_fp8_mma_probe": (ctypes.c_int, [_i32, _p, ctypes.POINTER(ctypes.c_double), _p, _p]),
 }
 
 
@@ -259,3 +261,12 @@ def idx_mxfp8_quantize(x, out, scales, stream=None) -> int:
     return _check("idx_mxfp8_quantize", lib.idx_mxfp8_quantize(
         _ptr(x), x.shape[0], x.shape[1], x.stride(0), _ptr(out), out.stride(0), _ptr(scales), scales.stride(0),
         _stream(stream)))
+
+
+def idx_fp8_mma_probe(iters: int, check=None, status=None, stream=None) -> float:
+    """Launch the dense FP8 tensor-core probe; returns the launch's floating-point operations."""
+    lib = load_library()
+    flops = ctypes.c_double(0.0)
+    _check("idx_fp8_mma_probe", lib.idx_fp8_mma_probe(int(iters), _ptr(check), ctypes.byref(flops), _ptr(status),
+                                                        _stream(stream)))
+    return float(flops.value)

@@ -58,6 +58,9 @@ def test_error_codes_and_strings(built):
     assert lib.idx_score_pages(16, 16, 16, 10, 16, 4, 4, 16, 2, 0, 4, 16, None, None) == E_SHAPE
     assert lib.idx_score_pages(8, 16, 16, 10, 16, 4, 4, 16, 2, 8, 4, 16, None, None) == E_MIS  # q not 16-aligned
     assert lib.idx_score_pages(16, 16, 16, 10, 16, 4, 4, 16, 0, 8, 4, 16, None, None) == 0  # no requests
+    assert lib.idx_fp8_mma_probe(0, None, None, None, None) == E_SHAPE  # iters 1 .. 100,000
+    assert lib.idx_fp8_mma_probe(100_001, None, None, None, None) == E_SHAPE
+    assert lib.idx_fp8_mma_probe(10, 2, None, None, None) == E_MIS  # check not 4-aligned
     assert lib.idx_topk16_select(16, 5000, 3, 5000, None, 0, 0, None, None, None, 0, None) == E_NULL
     assert lib.idx_topk16_select(16, 5000, 3, 5000, None, 0, 0, 16, None, None, 0, None) == E_WS
     assert lib.idx_topk16_select(16, 5000, 3, 5000, None, 0, 0, 16, None, 16, 8, None) == E_WS  # too small
