@@ -208,6 +208,9 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
     for (int k = 0; k < lane && k < count; ++k) pf.next();
     int64_t blk_l = lane < count ? (int64_t)bt[(int64_t)pf.r * bt_stride + pf.kb] : -1;
     int qord = -1, pr = -1, ptt = -1, issued = 0;  // qord: query tiles issued - 1
+    // key blocks are streamed through once: evict them first, so the score
+    // lines stay in L2 for the top-16 selection that follows
+    const uint64_t pol = l2_policy_evict_first();
     bool ok_all = true;
     for (int base = 0; base < count && ok_all; base += 32) {
       int64_t blk_next = -1;
@@ -247,7 +250,8 @@ __global__ void __launch_bounds__(kThreadsM, 2) k_mtp_tc(const __grid_constant__
             valid_ring[ks] = valid ? 1 : 0;
             if (valid) {
               mbar_arrive_expect_tx(&bars[kKFull + stage], kKTileBytes);
-              tma_load_2d(smem + kOffKm + stage * kKTileBytes, &kmap, 0, (int)(blk * kPageTokens), &bars[kKFull + stage]);
+              tma_load_2d_hint(smem + kOffKm + stage * kKTileBytes, &kmap, 0, (int)(blk * kPageTokens), &bars[kKFull + stage],
+                               pol);
               if (k_scale != nullptr) {
                 mbar_arrive_expect_tx(&bars[kKsFull + ks], kKsBytes);
                 bulk_g2s(smem + kOffKs + ks * kKsBytes, k_scale + blk * kPageTokens, kKsBytes, &bars[kKsFull + ks]);

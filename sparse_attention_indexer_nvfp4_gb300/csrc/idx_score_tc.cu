@@ -397,6 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     // without blocking, so a stage is refilled as soon as its dequant group
     // has loaded the page it held, whatever the other stages are doing.
     const bool owner = lane < kStages;
+    // the pages are read once: evict them first, so the score lines stay in
+    // L2 for the selector that follows
+    const uint64_t pol = l2_policy_evict_first();
     int gen = 0;              // pages with records
     int gb = b0, gj = j0;     // (request, page) of page `gen`
     int i = lane;             // the next page this lane copies
@@ -466,13 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
             // the unit's codes and scales, laid out in the stage as a P128 page
             const int h = recs[i % kRecs].j & 1;
             const uint8_t* src = kv + (int64_t)blk * (2 * kPageBytes);
-            bulk_g2s(smem + kOffRaw + lane * kPageBytes, src + h * kCodeBytes, kCodeBytes, &bars[kRawFull + lane]);
-            bulk_g2s(smem + kOffRaw + lane * kPageBytes + kCodeBytes,
-                     src + 2 * kCodeBytes + h * (kPageBytes - kCodeBytes), kPageBytes - kCodeBytes,
-                     &bars[kRawFull + lane]);
+            bulk_g2s_hint(smem + kOffRaw + lane * kPageBytes, src + h * kCodeBytes, kCodeBytes, &bars[kRawFull + lane],
+                          pol);
+            bulk_g2s_hint(smem + kOffRaw + lane * kPageBytes + kCodeBytes,
+                          src + 2 * kCodeBytes + h * (kPageBytes - kCodeBytes), kPageBytes - kCodeBytes,
+                          &bars[kRawFull + lane], pol);
           } else {
-            bulk_g2s(smem + kOffRaw + lane * kPageBytes, kv + (int64_t)blk * kPageBytes, kPageBytes,
-                     &bars[kRawFull + lane]);
+            bulk_g2s_hint(smem + kOffRaw + lane * kPageBytes, kv + (int64_t)blk * kPageBytes, kPageBytes,
+                          &bars[kRawFull + lane], pol);
           }
         } else {
           mbar_arrive(&bars[kRawFull + lane]);
@@ -514,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     const int slot_q = lane >> 2, iq = slot_q - (kSlots - query_len);
     int prev_b = -1, own = -1;
     float qs = 0.f;
+    const uint64_t keep = l2_policy_evict_last();  // the selector reads the scores next
     auto store_page = [&](int p) {
       const PageRec r = recs[p % kRecs];
       const float* sl = score_slots + score_slot(p) * 2 * kRows;
@@ -532,7 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
       }
       float val = qs >= 0.f ? qs * mx : qs * mn;
       if (!(r.blk >= 0 && r.blk < num_blocks)) val = __int_as_float(0x7FC00000);  // NaN: ranked as -inf
-      if (r.j < own) scores[((int64_t)r.b * kRows + lane) * (int64_t)(Geo<kP256>::kUnits * width) + r.j] = val;
+      if (r.j < own)
+        st_global_hint(scores + ((int64_t)r.b * kRows + lane) * (int64_t)(Geo<kP256>::kUnits * width) + r.j, val, keep);
     };
     bool issued_any = false, ok = true;
     int last = -1;  // the last page issued
