@@ -158,67 +158,105 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
   return result;
 }
 
-// Top-16 keys of columns [c0, c1) of one fp32 row (c1 - c0 <= 32 * K): the
-// 32-bit image pass, keys built only for survivors.  Lanes 0..15 hold the
-// result, descending, 0 padding.
+// Top-16 keys of columns [c0, c1) of one fp32 row (c1 - c0 <= 32 * K).
+// Lanes 0..15 hold the result, descending, 0 padding.
 // With rank16 every score is first rounded to binary16 (round to nearest
 // even, overflow to infinity) and widened back, so scores that tie in 16
 // bits rank by column.  With pair, column c's score is the max of row[2c]
 // and row[2c + 1] (a P256 page scored as two 128-key halves; row 8-byte
 // aligned).
+//
+// The scores stay floats in registers: a lane's maximum is fmaxf over its
+// columns (fmaxf drops NaN, and -0 and +0 have the same image, so its image
+// is the largest image of the lane), the threshold is the 16th largest of
+// the 32 lane-maximum images, and a column survives when its score compares
+// >= the threshold's float (NaN never does; -0 >= +0 holds), which is the
+// same test as image >= threshold whenever the threshold lies above the
+// image of -inf.  Images and keys are built for survivors only.  When the
+// threshold is at or below the image of -inf (fewer than 16 lanes hold a
+// column above -inf), the images of every column are compared instead,
+// with 0 for "no column".
 template <int K, bool kForce>
 __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
                                    bool rank16 = false, bool pair = false) {
   const uint32_t lane = lane_id();
   const uint32_t lt_mask = (1u << lane) - 1u;
-  const int nch = (c1 - c0 + 31) >> 5;
-  uint32_t u[K];
+  const int span = c1 - c0, lim = span - (int)lane;  // element i is a column iff 32 i < lim
+  const bool any_forced = kForce && fb < fe && fb < c1 && fe > c0;
+  const float kNoCol = __int_as_float(0x7FC00000);  // NaN: fmaxf skips it, >= never holds
+  float x[K];
+  float m = kNoCol;
 #pragma unroll
   for (int i = 0; i < K; ++i) {
-    const int col = c0 + i * 32 + (int)lane;
-    uint32_t v = 0;
-    if (i < nch && col < c1) {
-      float x;
+    float v = kNoCol;
+    if (32 * i < lim) {
+      const int col = c0 + i * 32 + (int)lane;
       if (pair) {
         const float2 h = __ldg(reinterpret_cast<const float2*>(row) + col);
-        x = fmaxf(h.x, h.y);
+        v = fmaxf(h.x, h.y);
       } else {
-        x = __ldg(row + col);
+        v = __ldg(row + col);
       }
-      if (rank16) x = __half2float(__float2half_rn(x));
-      v = ordered_bits(x);
-      if (kForce && col >= fb && col < fe) v = kOrderedPosInf;
+      if (rank16) v = __half2float(__float2half_rn(v));
+      if (any_forced && col >= fb && col < fe) v = INFINITY;
     }
-    u[i] = v;
+    x[i] = v;
+    m = fmaxf(m, v);
   }
-  uint32_t m = 0;
+  // a lane without a column has image 0, below every real score
+  uint32_t thr = __shfl_sync(kFull, warp_sort_desc_u32(lim > 0 ? ordered_bits(m) : 0u), 15);
+  // the images of every column, in place of the scores (x then holds bits)
+  auto to_images = [&]() {
 #pragma unroll
-  for (int i = 0; i < K; ++i) m = max(m, u[i]);
-  uint32_t thr = __shfl_sync(kFull, warp_sort_desc_u32(m), 15);
-  if (thr == 0) thr = 1;  // fewer than 16 columns: every one survives
+    for (int i = 0; i < K; ++i) x[i] = __uint_as_float(32 * i < lim ? ordered_bits(x[i]) : 0u);
+  };
 
   uint32_t count = 0;
+  bool images = false;
+  if (thr > ordered_bits(-INFINITY)) {
+    // the threshold's float: the inverse of the image map
+    const float t = __uint_as_float((thr & 0x80000000u) ? (thr ^ 0x80000000u) : ~thr);
 #pragma unroll
-  for (int i = 0; i < K; ++i) {
-    if (i < nch) {
-      const bool p = u[i] >= thr;
-      const uint32_t b = __ballot_sync(kFull, p);
-      if (b) {
-        const uint32_t pos = count + __popc(b & lt_mask);
-        if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(u[i], c0 + i * 32 + (int)lane);
-        count += __popc(b);
+    for (int i = 0; i < K; ++i) {
+      if (32 * i < span) {
+        const bool p = x[i] >= t;
+        const uint32_t b = __ballot_sync(kFull, p);
+        if (b) {
+          const uint32_t pos = count + __popc(b & lt_mask);
+          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(ordered_bits(x[i]), c0 + i * 32 + (int)lane);
+          count += __popc(b);
+        }
+      }
+    }
+  } else {
+    if (thr == 0) thr = 1;  // fewer than 16 columns: every one survives
+    to_images();
+    images = true;
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      if (32 * i < span) {
+        const uint32_t u = __float_as_uint(x[i]);
+        const bool p = u >= thr;
+        const uint32_t b = __ballot_sync(kFull, p);
+        if (b) {
+          const uint32_t pos = count + __popc(b & lt_mask);
+          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(u, c0 + i * 32 + (int)lane);
+          count += __popc(b);
+        }
       }
     }
   }
   __syncwarp();
   if (count <= (uint32_t)kMaxSurvivors) return rank_survivors(count, ws);
   // exact fallback (many equal images): 16 rounds over the full keys
+  if (!images) to_images();
   uint64_t result = 0, prev = ~0ull;
   for (int r = 0; r < kTopK; ++r) {
     uint64_t best = 0;
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-      const uint64_t key = u[i] ? key_from(u[i], c0 + i * 32 + (int)lane) : 0ull;
+      const uint32_t u = __float_as_uint(x[i]);
+      const uint64_t key = u ? key_from(u, c0 + i * 32 + (int)lane) : 0ull;
       best = (key < prev && key > best) ? key : best;
     }
     best = warp_max_u64(best);
