@@ -176,29 +176,68 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
 // threshold is at or below the image of -inf (fewer than 16 lanes hold a
 // column above -inf), the images of every column are compared instead,
 // with 0 for "no column".
-template <int K, bool kForce>
-__device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
-                                   bool rank16 = false, bool pair = false) {
+// Element i of a lane's K scores: column c0 + 32 i + lane (kVec false), or
+// c0 + 128 (i / 4) + 4 lane + i % 4 (kVec: one 16-byte load per four).
+template <bool kVec>
+__device__ __forceinline__ int seg_offset(int i, uint32_t lane) {
+  return kVec ? 128 * (i >> 2) + 4 * (int)lane + (i & 3) : 32 * i + (int)lane;
+}
+// whether any lane's element i can be a column (warp-uniform)
+template <bool kVec>
+__device__ __forceinline__ bool seg_slot(int i, int span) {
+  return kVec ? 128 * (i >> 2) < span : 32 * i < span;
+}
+
+template <int K, bool kForce, bool kVec>
+__device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
+                                        bool rank16, bool pair) {
+  static_assert(!kVec || K % 4 == 0, "16-byte loads take four scores at a time");
   const uint32_t lane = lane_id();
   const uint32_t lt_mask = (1u << lane) - 1u;
-  const int span = c1 - c0, lim = span - (int)lane;  // element i is a column iff 32 i < lim
+  const int span = c1 - c0;
+  // element i is a column iff its offset is below span: offset i = fixed(i) + lane part
+  const int lim = span - (kVec ? 4 * (int)lane : (int)lane);
+  auto fixed = [](int i) { return kVec ? 128 * (i >> 2) + (i & 3) : 32 * i; };
   const bool any_forced = kForce && fb < fe && fb < c1 && fe > c0;
   const float kNoCol = __int_as_float(0x7FC00000);  // NaN: fmaxf skips it, >= never holds
   float x[K];
+#pragma unroll
+  for (int i = 0; i < K; ++i) x[i] = kNoCol;
+  if (kVec) {
+#pragma unroll
+    for (int j = 0; j < K / 4; ++j) {
+      const int off = 128 * j + 4 * (int)lane;
+      if (off + 3 < span) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(row + c0 + off));
+        x[4 * j] = v.x, x[4 * j + 1] = v.y, x[4 * j + 2] = v.z, x[4 * j + 3] = v.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (off + e < span) x[4 * j + e] = __ldg(row + c0 + off + e);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      if (fixed(i) < lim) {
+        const int col = c0 + i * 32 + (int)lane;
+        if (pair) {
+          const float2 h = __ldg(reinterpret_cast<const float2*>(row) + col);
+          x[i] = fmaxf(h.x, h.y);
+        } else {
+          x[i] = __ldg(row + col);
+        }
+      }
+    }
+  }
   float m = kNoCol;
 #pragma unroll
   for (int i = 0; i < K; ++i) {
-    float v = kNoCol;
-    if (32 * i < lim) {
-      const int col = c0 + i * 32 + (int)lane;
-      if (pair) {
-        const float2 h = __ldg(reinterpret_cast<const float2*>(row) + col);
-        v = fmaxf(h.x, h.y);
-      } else {
-        v = __ldg(row + col);
-      }
-      if (rank16) v = __half2float(__float2half_rn(v));
-      if (any_forced && col >= fb && col < fe) v = INFINITY;
+    float v = x[i];
+    if (rank16) v = __half2float(__float2half_rn(v));
+    if (any_forced) {
+      const int col = c0 + seg_offset<kVec>(i, lane);
+      if (fixed(i) < lim && col >= fb && col < fe) v = INFINITY;
     }
     x[i] = v;
     m = fmaxf(m, v);
@@ -208,7 +247,7 @@ __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1
   // the images of every column, in place of the scores (x then holds bits)
   auto to_images = [&]() {
 #pragma unroll
-    for (int i = 0; i < K; ++i) x[i] = __uint_as_float(32 * i < lim ? ordered_bits(x[i]) : 0u);
+    for (int i = 0; i < K; ++i) x[i] = __uint_as_float(fixed(i) < lim ? ordered_bits(x[i]) : 0u);
   };
 
   uint32_t count = 0;
@@ -218,12 +257,12 @@ __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1
     const float t = __uint_as_float((thr & 0x80000000u) ? (thr ^ 0x80000000u) : ~thr);
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-      if (32 * i < span) {
+      if (seg_slot<kVec>(i, span)) {
         const bool p = x[i] >= t;
         const uint32_t b = __ballot_sync(kFull, p);
         if (b) {
           const uint32_t pos = count + __popc(b & lt_mask);
-          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(ordered_bits(x[i]), c0 + i * 32 + (int)lane);
+          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(ordered_bits(x[i]), c0 + seg_offset<kVec>(i, lane));
           count += __popc(b);
         }
       }
@@ -234,13 +273,13 @@ __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1
     images = true;
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-      if (32 * i < span) {
+      if (seg_slot<kVec>(i, span)) {
         const uint32_t u = __float_as_uint(x[i]);
         const bool p = u >= thr;
         const uint32_t b = __ballot_sync(kFull, p);
         if (b) {
           const uint32_t pos = count + __popc(b & lt_mask);
-          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(u, c0 + i * 32 + (int)lane);
+          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(u, c0 + seg_offset<kVec>(i, lane));
           count += __popc(b);
         }
       }
@@ -256,7 +295,7 @@ __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1
 #pragma unroll
     for (int i = 0; i < K; ++i) {
       const uint32_t u = __float_as_uint(x[i]);
-      const uint64_t key = u ? key_from(u, c0 + i * 32 + (int)lane) : 0ull;
+      const uint64_t key = u ? key_from(u, c0 + seg_offset<kVec>(i, lane)) : 0ull;
       best = (key < prev && key > best) ? key : best;
     }
     best = warp_max_u64(best);
@@ -266,6 +305,17 @@ __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1
   }
   __syncwarp();
   return result;
+}
+
+// Rows whose segment starts on a 16-byte boundary take 16-byte loads (four
+// scores per instruction); paired columns and other rows take one load per
+// column.
+template <int K, bool kForce>
+__device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
+                                   bool rank16 = false, bool pair = false) {
+  if (K % 4 == 0 && !pair && (reinterpret_cast<uintptr_t>(row + c0) & 15u) == 0)
+    return warp_top16_seg_impl<K, kForce, (K % 4 == 0)>(row, c0, c1, fb, fe, ws, rank16, pair);
+  return warp_top16_seg_impl<K, kForce, false>(row, c0, c1, fb, fe, ws, rank16, pair);
 }
 
 }  // namespace sel
