@@ -58,14 +58,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // nsplit CTAs whose top-16s are merged through the workspace.
 constexpr int kMaxPerLane = 64;
 constexpr int kWideWarpTarget = 1216;  // 8 warps per SM: below this, halve the segments
-// Few rows of moderate width (fewer than 16 per SM of the GPU, 257 to 1,536
-// columns): four warps per row, 12 values per lane each, merged in shared
-// memory, so that a row's chain is a quarter as long and the GPU holds four
-// times as many warps.  The choice never splits a row across CTAs, so the
-// workspace a row shape needs does not depend on it (or on the GPU).
-constexpr int kSplitPerLane = 12;
-constexpr int kFewRowsPerSm = 16;
-
 // Streaming multiprocessors of the current device (cached per device; 0 when
 // the query fails).
 int device_sms();
@@ -76,12 +68,9 @@ struct RowSplit {
   int nsplit;    // CTAs per row
 };
 
-// few_rows: the row count below which moderate rows take four warps
-// (kFewRowsPerSm per SM of the GPU that runs the launch; 0 never).
-inline RowSplit row_split(int64_t rows, int32_t width, int64_t few_rows = 0) {
+inline RowSplit row_split(int64_t rows, int32_t width) {
   const int64_t w = width <= 0 ? 1 : width;
   if (w <= 32 * kMaxPerLane) {
-    if (w > 256 && w <= 4 * 32 * kSplitPerLane && rows < few_rows) return RowSplit{kSplitPerLane, 4, 1};
     const int need = (int)((w + 31) / 32);
     const int per_lane = need <= 8 ? 8 : need <= 16 ? 16 : need <= 32 ? 32 : need <= 48 ? 48 : 64;
     return RowSplit{per_lane, 1, 1};

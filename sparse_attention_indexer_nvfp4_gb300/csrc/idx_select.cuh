@@ -158,6 +158,18 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
   return result;
 }
 
+// Element i of a lane's K scores: column c0 + 32 i + lane (kVec false), or
+// c0 + 128 (i / 4) + 4 lane + i % 4 (kVec: one 16-byte load per four).
+template <bool kVec>
+__device__ __forceinline__ int seg_offset(int i, uint32_t lane) {
+  return kVec ? 128 * (i >> 2) + 4 * (int)lane + (i & 3) : 32 * i + (int)lane;
+}
+// whether any lane's element i can be a column (warp-uniform)
+template <bool kVec>
+__device__ __forceinline__ bool seg_slot(int i, int span) {
+  return kVec ? 128 * (i >> 2) < span : 32 * i < span;
+}
+
 // Top-16 keys of columns [c0, c1) of one fp32 row (c1 - c0 <= 32 * K).
 // Lanes 0..15 hold the result, descending, 0 padding.
 // With rank16 every score is first rounded to binary16 (round to nearest
@@ -176,18 +188,6 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
 // threshold is at or below the image of -inf (fewer than 16 lanes hold a
 // column above -inf), the images of every column are compared instead,
 // with 0 for "no column".
-// Element i of a lane's K scores: column c0 + 32 i + lane (kVec false), or
-// c0 + 128 (i / 4) + 4 lane + i % 4 (kVec: one 16-byte load per four).
-template <bool kVec>
-__device__ __forceinline__ int seg_offset(int i, uint32_t lane) {
-  return kVec ? 128 * (i >> 2) + 4 * (int)lane + (i & 3) : 32 * i + (int)lane;
-}
-// whether any lane's element i can be a column (warp-uniform)
-template <bool kVec>
-__device__ __forceinline__ bool seg_slot(int i, int span) {
-  return kVec ? 128 * (i >> 2) < span : 32 * i < span;
-}
-
 template <int K, bool kForce, bool kVec>
 __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
                                         bool rank16, bool pair) {

@@ -190,7 +190,7 @@ void launch_k(const PlainRows& p, const DecodeRows& d, int64_t rows, int nsplit,
 
 template <bool kDecode>
 int launch_rows(const PlainRows& p, const DecodeRows& d, int64_t rows, int32_t width, void* ws, cudaStream_t s) {
-  const RowSplit sp = row_split(rows, width, (int64_t)device_sms() * kFewRowsPerSm);
+  const RowSplit sp = row_split(rows, width);
   if (sp.nsplit > 65535) return IDX_E_TOO_LARGE;
   if (rows > 0x7FFFFFFFLL) return IDX_E_TOO_LARGE;
   uint64_t* wsk = static_cast<uint64_t*>(ws);
@@ -209,9 +209,7 @@ int launch_rows(const PlainRows& p, const DecodeRows& d, int64_t rows, int32_t w
     else
       launch_k<kDecode, 2, 64>(p, d, rows, sp.nsplit, wsk, s);
   } else {
-    if (sp.per_lane == kSplitPerLane)
-      launch_k<kDecode, 4, kSplitPerLane>(p, d, rows, sp.nsplit, wsk, s);
-    else if (sp.per_lane == 32)
+    if (sp.per_lane == 32)
       launch_k<kDecode, 4, 32>(p, d, rows, sp.nsplit, wsk, s);
     else
       launch_k<kDecode, 4, 64>(p, d, rows, sp.nsplit, wsk, s);
