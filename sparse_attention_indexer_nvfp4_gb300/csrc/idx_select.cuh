@@ -158,16 +158,17 @@ __device__ uint64_t warp_top16_update(const uint64_t (&k)[K], uint64_t run, Warp
   return result;
 }
 
-// Element i of a lane's K scores: column c0 + 32 i + lane (kVec false), or
-// c0 + 128 (i / 4) + 4 lane + i % 4 (kVec: one 16-byte load per four).
-template <bool kVec>
+// Element i of a lane's K scores, with kW columns per 16-byte load (1: one
+// load per column; 4: four columns; 2: two paired columns, eight floats):
+// column c0 + 32 kW (i / kW) + kW lane + i % kW.
+template <int kW>
 __device__ __forceinline__ int seg_offset(int i, uint32_t lane) {
-  return kVec ? 128 * (i >> 2) + 4 * (int)lane + (i & 3) : 32 * i + (int)lane;
+  return 32 * kW * (i / kW) + kW * (int)lane + (i % kW);
 }
 // whether any lane's element i can be a column (warp-uniform)
-template <bool kVec>
+template <int kW>
 __device__ __forceinline__ bool seg_slot(int i, int span) {
-  return kVec ? 128 * (i >> 2) < span : 32 * i < span;
+  return 32 * kW * (i / kW) < span;
 }
 
 // Top-16 keys of columns [c0, c1) of one fp32 row (c1 - c0 <= 32 * K).
@@ -188,22 +189,22 @@ __device__ __forceinline__ bool seg_slot(int i, int span) {
 // threshold is at or below the image of -inf (fewer than 16 lanes hold a
 // column above -inf), the images of every column are compared instead,
 // with 0 for "no column".
-template <int K, bool kForce, bool kVec>
+template <int K, bool kForce, int kW>
 __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
                                         bool rank16, bool pair) {
-  static_assert(!kVec || K % 4 == 0, "16-byte loads take four scores at a time");
+  static_assert(K % kW == 0, "16-byte loads fill kW elements at a time");
   const uint32_t lane = lane_id();
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int span = c1 - c0;
-  // element i is a column iff its offset is below span: offset i = fixed(i) + lane part
-  const int lim = span - (kVec ? 4 * (int)lane : (int)lane);
-  auto fixed = [](int i) { return kVec ? 128 * (i >> 2) + (i & 3) : 32 * i; };
+  // element i is a column iff its offset is below span: offset i = fixed(i) + kW lane
+  const int lim = span - kW * (int)lane;
+  auto fixed = [](int i) { return 32 * kW * (i / kW) + (i % kW); };
   const bool any_forced = kForce && fb < fe && fb < c1 && fe > c0;
   const float kNoCol = __int_as_float(0x7FC00000);  // NaN: fmaxf skips it, >= never holds
   float x[K];
 #pragma unroll
   for (int i = 0; i < K; ++i) x[i] = kNoCol;
-  if (kVec) {
+  if (kW == 4) {
 #pragma unroll
     for (int j = 0; j < K / 4; ++j) {
       const int off = 128 * j + 4 * (int)lane;
@@ -214,6 +215,20 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           if (off + e < span) x[4 * j + e] = __ldg(row + c0 + off + e);
+      }
+    }
+  } else if (kW == 2) {
+    // paired columns: column c is the max of row[2c] and row[2c + 1]
+    const float2* row2 = reinterpret_cast<const float2*>(row);
+#pragma unroll
+    for (int j = 0; j < K / 2; ++j) {
+      const int off = 64 * j + 2 * (int)lane;
+      if (off + 1 < span) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(row2 + c0 + off));
+        x[2 * j] = fmaxf(v.x, v.y), x[2 * j + 1] = fmaxf(v.z, v.w);
+      } else if (off < span) {
+        const float2 h = __ldg(row2 + c0 + off);
+        x[2 * j] = fmaxf(h.x, h.y);
       }
     }
   } else {
@@ -236,7 +251,7 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
     float v = x[i];
     if (rank16) v = __half2float(__float2half_rn(v));
     if (any_forced) {
-      const int col = c0 + seg_offset<kVec>(i, lane);
+      const int col = c0 + seg_offset<kW>(i, lane);
       if (fixed(i) < lim && col >= fb && col < fe) v = INFINITY;
     }
     x[i] = v;
@@ -257,12 +272,12 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
     const float t = __uint_as_float((thr & 0x80000000u) ? (thr ^ 0x80000000u) : ~thr);
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-      if (seg_slot<kVec>(i, span)) {
+      if (seg_slot<kW>(i, span)) {
         const bool p = x[i] >= t;
         const uint32_t b = __ballot_sync(kFull, p);
         if (b) {
           const uint32_t pos = count + __popc(b & lt_mask);
-          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(ordered_bits(x[i]), c0 + seg_offset<kVec>(i, lane));
+          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(ordered_bits(x[i]), c0 + seg_offset<kW>(i, lane));
           count += __popc(b);
         }
       }
@@ -273,13 +288,13 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
     images = true;
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-      if (seg_slot<kVec>(i, span)) {
+      if (seg_slot<kW>(i, span)) {
         const uint32_t u = __float_as_uint(x[i]);
         const bool p = u >= thr;
         const uint32_t b = __ballot_sync(kFull, p);
         if (b) {
           const uint32_t pos = count + __popc(b & lt_mask);
-          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(u, c0 + seg_offset<kVec>(i, lane));
+          if (p && pos < kMaxSurvivors) ws->surv[pos] = key_from(u, c0 + seg_offset<kW>(i, lane));
           count += __popc(b);
         }
       }
@@ -295,7 +310,7 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
 #pragma unroll
     for (int i = 0; i < K; ++i) {
       const uint32_t u = __float_as_uint(x[i]);
-      const uint64_t key = u ? key_from(u, c0 + seg_offset<kVec>(i, lane)) : 0ull;
+      const uint64_t key = u ? key_from(u, c0 + seg_offset<kW>(i, lane)) : 0ull;
       best = (key < prev && key > best) ? key : best;
     }
     best = warp_max_u64(best);
@@ -307,15 +322,17 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
   return result;
 }
 
-// Rows whose segment starts on a 16-byte boundary take 16-byte loads (four
-// scores per instruction); paired columns and other rows take one load per
-// column.
+// Segments that start on a 16-byte boundary take 16-byte loads (four
+// scores, or two paired columns, per instruction); others one load per column.
 template <int K, bool kForce>
 __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
                                    bool rank16 = false, bool pair = false) {
-  if (K % 4 == 0 && !pair && (reinterpret_cast<uintptr_t>(row + c0) & 15u) == 0)
-    return warp_top16_seg_impl<K, kForce, (K % 4 == 0)>(row, c0, c1, fb, fe, ws, rank16, pair);
-  return warp_top16_seg_impl<K, kForce, false>(row, c0, c1, fb, fe, ws, rank16, pair);
+  constexpr int kW4 = K % 4 == 0 ? 4 : 1, kW2 = K % 2 == 0 ? 2 : 1;
+  if (!pair && (reinterpret_cast<uintptr_t>(row + c0) & 15u) == 0)
+    return warp_top16_seg_impl<K, kForce, kW4>(row, c0, c1, fb, fe, ws, rank16, pair);
+  if (pair && (reinterpret_cast<uintptr_t>(row + 2 * c0) & 15u) == 0)
+    return warp_top16_seg_impl<K, kForce, kW2>(row, c0, c1, fb, fe, ws, rank16, pair);
+  return warp_top16_seg_impl<K, kForce, 1>(row, c0, c1, fb, fe, ws, rank16, pair);
 }
 
 }  // namespace sel
