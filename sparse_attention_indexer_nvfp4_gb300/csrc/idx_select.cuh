@@ -1,5 +1,5 @@
-// Warp-level exact top-16 primitives over 64-bit page keys, shared by the
-// top-16 selector and the decode scorer's fused selection.
+// Warp-level exact top-16 primitives over 64-bit page keys, used by the
+// top-16 selector kernels.
 //
 // Selection follows "wolfcomos/MSA PR #1" (section Changes): one warp ranks a
 // run of columns; every lane takes its largest key, every key at or above the
@@ -8,12 +8,11 @@
 // counting the survivors above it, so the result does not depend on slot
 // order; with more than 64 survivors the warp falls back to 16 exact rounds.
 //
-// The first pass over a run of scores works on the 32-bit order-preserving
-// image of each score (the upper half of its key) and builds full keys only
-// for survivors: the threshold is the 16th largest lane maximum of those
-// images, so every key of the top 16 still survives (16 lane maxima lie at
-// or above it, each a distinct key at least as large), ties in the image
-// only add survivors.
+// The threshold is taken on the 32-bit order-preserving image of each score
+// (the upper half of its key): every key of the top 16 still survives (16
+// lane maxima lie at or above the threshold, each a distinct key at least as
+// large), and ties in the image only add survivors.  Full keys are built
+// for survivors only.
 #pragma once
 
 #include "idx_common.cuh"
