@@ -57,7 +57,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // (with 1 warp per row, a CTA carries 4 rows); wider rows split across
 // nsplit CTAs whose top-16s are merged through the workspace.
 constexpr int kMaxPerLane = 64;
-constexpr int kWideWarpTarget = 1216;  // 8 warps per SM: below this, halve the segments
+// Rows wider than one warp's 2,048 columns: when fewer than this many warps
+// would run (8 per SM of a 152-SM GB300), the segments are halved to 1,024
+// columns.  It fixes the split, so workspace sizes (idx_workspace_bytes,
+// which takes no device) depend on it; it is a tuning constant, not the
+// device's SM count.
+constexpr int kWideWarpTarget = 1216;
 // Streaming multiprocessors of the current device (cached per device; 0 when
 // the query fails).
 int device_sms();
