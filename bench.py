@@ -54,12 +54,13 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-# Sources each kernel is built from (its own file plus the shared headers).
+# Sources each kernel is built from (its own file and the headers it
+# includes beyond the shared ones).
 KERNEL_SOURCES = {
-    "k_score_decode": ["idx_score_tc.cu"],
-    "k_topk_rows": ["idx_topk.cu"],
-    "k_mtp_tc": ["idx_mtp_tc.cu"],
-    "k_dequant_nvfp4": ["idx_dequant.cu"],
+    "k_score_decode": ["idx_score_tc.cu", "idx_fused.cuh", "idx_select.cuh", "idx_internal.h"],
+    "k_topk_rows": ["idx_topk.cu", "idx_select.cuh", "idx_internal.h"],
+    "k_mtp_tc": ["idx_mtp_tc.cu", "idx_internal.h"],
+    "k_dequant_nvfp4": ["idx_dequant.cu", "idx_internal.h"],
 }
 SHARED_SOURCES = ["idx_common.cuh", "idx_tc.cuh", "../../include/idx.h"]  # device code the kernels include
 
@@ -569,6 +570,46 @@ def secondary(args, torch, idx, W, timer, hbm_peak, main) -> dict:
                               "ms_step": step1, "ms_scorer": score, "scores_per_s": u1["scores"] / (step1 / 1e3),
                               "index_k_gbs": u1["pages"] * PAGE_BYTES / (score / 1e3) / 1e9}
 
+    if "fused" in args.legs:
+        # the fused decode step (selection in the scorer's CTAs, one launch)
+        # against the two-launch step, alternating, on the main workload and
+        # the long-context one; rows must be identical
+        res["fused"] = {}
+        for name in ("batched", "long_context"):
+            if name == "batched":
+                wl, q, qs, kv, bt, sl = main["wl"], main["q"], main["qs"], main["kv"], main["bt"], main["sl"]
+            else:
+                wl = W.long_context()
+                q, qs, kv, bt, sl = (to_dev(wl[k]) for k in ("q", "q_scale", "kv", "bt", "seq_lens"))
+            B, width = len(wl["seq_lens"]), wl["width"]
+            sc = torch.empty((B, 32, width), dtype=torch.float32, device="cuda")
+            out_c = torch.empty((B, 8, 4, 16), dtype=torch.int32, device="cuda")
+            out_f = torch.full_like(out_c, -7)
+            wsb = idx.idx_decode_workspace_bytes(B, 8, width)
+            ws = torch.empty(max(8, wsb) // 8, dtype=torch.int64, device="cuda") if wsb else None
+            wsf = torch.zeros(idx.idx_decode_fused_workspace_bytes(B) // 8, dtype=torch.int64, device="cuda")
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            chain = lambda: idx.idx_decode_step(q, qs, kv, bt, sl, 8, sc, out_c, ws, st)
+            fused = lambda: idx.idx_decode_step(q, qs, kv, bt, sl, 8, sc, out_f, wsf, st, flags=idx.FUSED_SELECT)
+            chain()
+            fused()
+            torch.cuda.synchronize()
+            same = bool(torch.equal(out_c, out_f)) and int(st.item()) == 0
+            tc, tf = [], []
+            for _ in range(3):
+                tc.append(timer.run(chain, iters))
+                tf.append(timer.run(fused, iters))
+            same = same and bool(torch.equal(out_c, out_f)) and int(wsf[: (B + 1) // 2].abs().sum().item()) == 0
+            u = decode_units(wl)
+            mc, mf = statistics.median(tc), statistics.median(tf)
+            res["fused"][name] = {"ms_two_launch": mc, "ms_fused": mf, "rows_identical": same,
+                                  "fused_frac_of_hbm": u["pages"] * PAGE_BYTES / (mf / 1e3) / 1e9 / hbm_peak,
+                                  "launches_fused": 1, "launches_two_launch": 2 + (1 if wsb else 0)}
+            if name != "batched":
+                del q, qs, kv, bt, sl
+            del sc, out_c, out_f, ws, wsf, wl
+            torch.cuda.empty_cache()
+
     if "p256" in args.legs:
         # the batched decode on P256 pages: 672-column rows, each page scored as two 128-key halves
         wl = W.batched_decode(page_tokens=256)
@@ -721,7 +762,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip secondary workloads; short CPU baseline")
-    ap.add_argument("--legs", default="fp8,gather,long,mtp,prefill,p256,tiny,qlen1,sweep,mxfp8",
+    ap.add_argument("--legs", default="fp8,gather,long,mtp,prefill,p256,fused,tiny,qlen1,sweep,mxfp8",
                     help="secondary workloads to time (comma list of fp8, gather, long, mtp, prefill, p256, tiny, qlen1, "
                          "sweep, mxfp8; empty for none)")
     args = ap.parse_args()

@@ -235,16 +235,38 @@ int idx_topk16_select_noalloc(const float* scores, int64_t row_stride, int32_t r
  *                 [128h, 128h+128) of page j (stored where page j is, i.e.
  *                 below the own page), and the page's score is the larger
  *                 of the pair.
+ *                 IDX_FUSED_SELECT: the selection runs in the scorer's own
+ *                 CTAs, with no second launch ([CP] module docstring: a
+ *                 local top 16 per page range, merged exactly over the
+ *                 union).  Each CTA ranks the pages of its slice per
+ *                 (request, row) from its own score stores, and the CTA
+ *                 that finishes a request last merges the local top-16s
+ *                 into the rows.  The rows are identical to the two-launch
+ *                 step's.  workspace is then >=
+ *                 idx_decode_fused_workspace_bytes(num_reqs) bytes, 8-byte
+ *                 aligned, and ZERO-FILLED before its first use: it holds
+ *                 per-request counters that every complete call leaves at
+ *                 zero again (zero it again after a call whose status
+ *                 reports IDX_ST_TIMEOUT, or before reusing it for another
+ *                 purpose).  Not with IDX_PAGE_256 (IDX_E_BAD_SHAPE).
  *                 Other bits: IDX_E_BAD_SHAPE.
  * Other arguments as in idx_score_pages.
  *
  * idx_decode_workspace_bytes: the selector's workspace for the step's
  * num_reqs * query_len * 4 rows of `width` columns, i.e.
  * idx_workspace_bytes(num_reqs * query_len * 4, width); 0 for a bad shape.
+ *
+ * idx_decode_fused_workspace_bytes: the workspace of a step with
+ * IDX_FUSED_SELECT: 4 bytes of counter per request (rounded up to 256
+ * bytes), then (num_reqs + 512) * 32 * 16 candidate keys of 8 bytes (the
+ * fused scorer runs at most 512 CTAs); 0 when num_reqs is outside
+ * [1, 65535].
  */
 size_t idx_decode_workspace_bytes(int32_t num_reqs, int32_t query_len, int32_t width);
+size_t idx_decode_fused_workspace_bytes(int32_t num_reqs);
 #define IDX_RANK_16BIT 1
 #define IDX_PAGE_256 2
+#define IDX_FUSED_SELECT 4
 int idx_decode_step(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
                     const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                     const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,

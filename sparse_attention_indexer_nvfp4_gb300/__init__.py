@@ -21,6 +21,7 @@ __all__ = [
     "idx_have_qmul4",
     "idx_workspace_bytes",
     "idx_decode_workspace_bytes",
+    "idx_decode_fused_workspace_bytes",
     "idx_set_wait_limit",
     "DEFAULT_WAIT_POLLS",
     "idx_dequant_nvfp4_pages",
@@ -31,6 +32,7 @@ __all__ = [
     "idx_decode_step",
     "RANK_16BIT",
     "PAGE_256",
+    "FUSED_SELECT",
     "idx_mtp_score_fp8",
     "idx_prefill_workspace_bytes",
     "idx_prefill_index_step",
@@ -65,6 +67,7 @@ SYMBOLS = {
     "idx_have_qmul4": (ctypes.c_int, []),
     "idx_workspace_bytes": (_sz, [_i32, _i32]),
     "idx_decode_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "idx_decode_fused_workspace_bytes": (_sz, [_i32]),
     "idx_set_wait_limit": (ctypes.c_uint32, [ctypes.c_uint32]),
     "idx_dequant_nvfp4_pages": (ctypes.c_int, [_p, _i64, _p, _i64, _i32, _p, _p, _i32, _i32, _p, _i64, _p, _p]),
     "idx_score_pages": (ctypes.c_int, [_p, _p, _p, _i64, _p, _i64, _i32, _p, _i32, _i32, _i32, _p, _p, _p]),
@@ -164,6 +167,11 @@ def idx_decode_workspace_bytes(num_reqs: int, query_len: int, width: int) -> int
     return int(load_library().idx_decode_workspace_bytes(num_reqs, query_len, width))
 
 
+def idx_decode_fused_workspace_bytes(num_reqs: int) -> int:
+    """Workspace of a decode step with FUSED_SELECT (zero-filled before its first use)."""
+    return int(load_library().idx_decode_fused_workspace_bytes(num_reqs))
+
+
 def idx_set_wait_limit(polls: int) -> int:
     """Set the tensor-core kernels' pipeline-wait budget (suspended polls); returns the previous one."""
     return int(load_library().idx_set_wait_limit(int(polls)))
@@ -214,6 +222,7 @@ def idx_topk16_select_noalloc(scores, out_idx, valid_n=None, force_begin: int = 
 
 RANK_16BIT = 1  # idx_decode_step flag: rank the scores rounded to binary16
 PAGE_256 = 2  # idx_decode_step flag: P256 pages (scores_ws [B, 32, 2 * width], a page the max of a column pair)
+FUSED_SELECT = 4  # idx_decode_step flag: selection inside the scorer's CTAs (zero-filled fused workspace)
 
 
 def idx_decode_step(q, q_scale, kv, block_table, seq_lens, query_len: int, scores_ws, out, workspace=None,

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "idx_common.cuh"
+#include "idx_fused.cuh"
 #include "idx_internal.h"
 
 namespace idx {
@@ -14,7 +15,7 @@ namespace idx {
 int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
                     int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream,
-                    int32_t page_tokens);
+                    int32_t page_tokens, int32_t* fused_out, void* fused_ws, bool rank16);
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -92,7 +93,7 @@ int launch_score_pages(const uint8_t* q, const float* q_scale, const uint8_t* kv
                        int32_t num_reqs, int32_t query_len, int32_t width, float* scores, int32_t* status,
                        cudaStream_t stream, int32_t page_tokens) {
   return launch_score_tc(q, q_scale, kv, num_blocks, bt, bt_stride, max_blocks, seq_lens, num_reqs, query_len, width,
-                         scores, status, stream, page_tokens);
+                         scores, status, stream, page_tokens, nullptr, nullptr, false);
 }
 
 namespace {
@@ -154,6 +155,11 @@ extern "C" size_t idx_decode_workspace_bytes(int32_t num_reqs, int32_t query_len
   return idx::topk_workspace_bytes(num_reqs * query_len * idx::kHeads, width);
 }
 
+extern "C" size_t idx_decode_fused_workspace_bytes(int32_t num_reqs) {
+  if (num_reqs <= 0 || num_reqs > 65535) return 0;
+  return idx::fused::workspace_bytes(num_reqs);
+}
+
 extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks,
                                const int32_t* block_table, int64_t bt_stride, int32_t max_blocks,
                                const int32_t* seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
@@ -161,7 +167,9 @@ extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uin
                                int32_t flags, int32_t* status, void* stream) {
   using namespace idx;
   if (num_reqs < 0 || width < 0 || max_blocks < 0 || query_len < 1 || query_len > kSlots) return IDX_E_BAD_SHAPE;
-  if ((flags & ~(IDX_RANK_16BIT | IDX_PAGE_256)) != 0) return IDX_E_BAD_SHAPE;
+  if ((flags & ~(IDX_RANK_16BIT | IDX_PAGE_256 | IDX_FUSED_SELECT)) != 0) return IDX_E_BAD_SHAPE;
+  const bool fuse = (flags & IDX_FUSED_SELECT) != 0;
+  if (fuse && (flags & IDX_PAGE_256)) return IDX_E_BAD_SHAPE;
   if (num_reqs == 0) return IDX_OK;
   if (!out || !seq_lens) return IDX_E_NULL_PTR;
   const int32_t page_tokens = (flags & IDX_PAGE_256) ? 2 * kPageTokens : kPageTokens;
@@ -175,10 +183,20 @@ extern "C" int idx_decode_step(const uint8_t* q, const float* q_scale, const uin
                           query_len, width, scores_ws);
     if (rc != IDX_OK) return rc;
   }
-  const size_t need = idx_decode_workspace_bytes(num_reqs, query_len, width);
+  const size_t need = fuse ? idx_decode_fused_workspace_bytes(num_reqs) : idx_decode_workspace_bytes(num_reqs, query_len, width);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return IDX_E_WORKSPACE;
   if ((rc = check_device()) != IDX_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;
+  if (fuse && any_pages)
+    return launch_score_tc(q, q_scale, kv, num_blocks, block_table, bt_stride, max_blocks, seq_lens, num_reqs,
+                           query_len, width, scores_ws, status, s, kPageTokens, out, workspace,
+                           (flags & IDX_RANK_16BIT) != 0);
+  if (fuse) {
+    // no page is scored: every row is assembled without ranking (width 0
+    // keeps the selector off the workspace, which holds the counters)
+    DecodeRows d{scores_ws, seq_lens, num_reqs, query_len, 0, 0, out, (flags & IDX_RANK_16BIT) != 0, kPageTokens};
+    return launch_topk_decode(d, nullptr, s);
+  }
   if (any_pages) {
     rc = launch_score_pages(q, q_scale, kv, num_blocks, block_table, bt_stride, max_blocks, seq_lens, num_reqs,
                             query_len, width, scores_ws, status, s, page_tokens);

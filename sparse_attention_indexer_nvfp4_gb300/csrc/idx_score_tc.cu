@@ -82,6 +82,7 @@
 // records IDX_ST_TIMEOUT, winds down, waits for its own copies and MMAs, and
 // frees its TMEM.
 #include "idx_common.cuh"
+#include "idx_fused.cuh"
 #include "idx_internal.h"
 #include "idx_tc.cuh"
 
@@ -287,12 +288,14 @@ __device__ __forceinline__ int ld_acquire_shared(const int* p) {
   return v;
 }
 
-template <bool kP256>
+// kFused: the decode step's selection follows the scoring in the same CTAs
+// (idx_fused.cuh); the rows go to fa.out.
+template <bool kP256, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     const uint8_t* __restrict__ q, const float* __restrict__ q_scale, const uint8_t* __restrict__ kv,
     int64_t num_blocks, const int32_t* __restrict__ bt, int64_t bt_stride, int32_t max_blocks,
     const int32_t* __restrict__ seq_lens, int32_t num_reqs, int32_t query_len, int32_t width,
-    float* __restrict__ scores, int32_t* status, uint32_t wait_polls) {
+    float* __restrict__ scores, int32_t* status, uint32_t wait_polls, fused::Args fa) {
   pdl_enter();  // before any global-memory access
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -335,7 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
   const unsigned long long P = misc->total;
   const unsigned long long p0 = P * blockIdx.x / gridDim.x, p1 = P * (blockIdx.x + 1) / gridDim.x;
   const int count = (int)(p1 - p0);
-  if (count == 0) return;  // uniform across the CTA
+  if (count == 0) {  // uniform across the CTA
+    if (kFused)
+      fused::zero_page_rows<kThreads / 32>(fa, fused::PageCounts{req_pages, kReqCache, seq_lens, cap}, seq_lens,
+                                           num_reqs, query_len);
+    return;
+  }
   if (warp == 1) {
     unsigned long long acc = 0;
     for (int base = 0; base < num_reqs; base += 32) {
@@ -733,16 +741,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_decode(
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (kFused) {
+    // The raw ring is idle: every copy into it has completed.  The slice is
+    // read again from shared memory (volatile), so that none of its values
+    // has to stay in a register through the pipeline above.
+    const volatile Misc* vm = misc;
+    const unsigned long long Pt = vm->total;
+    const unsigned long long p0t = Pt * blockIdx.x / gridDim.x;
+    const int count_t = (int)(Pt * (blockIdx.x + 1) / gridDim.x - p0t);
+    const fused::PageCounts counts{req_pages, kReqCache, seq_lens, min(max_blocks, width)};
+    fused::zero_page_rows<kThreads / 32>(fa, counts, seq_lens, num_reqs, query_len);
+    fused::slice_rows<kThreads / 32>(fa, counts, scores, width, seq_lens, num_reqs, query_len, Pt, p0t, count_t, vm->b0,
+                                     vm->j0, *reinterpret_cast<fused::TailShared<kThreads / 32>*>(smem + kOffRaw));
+  }
 }
+static_assert(sizeof(fused::TailShared<kThreads / 32>) <= kStages * kPageBytes, "the tail's shared memory fits the raw ring");
 
 int g_sms[64];
 bool g_attr[64];
 
-template <bool kP256>
+template <bool kP256, bool kFused>
 bool set_attrs() {
-  return cudaFuncSetAttribute(k_score_decode<kP256>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) ==
-             cudaSuccess &&
-         cudaFuncSetAttribute(k_score_decode<kP256>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  return cudaFuncSetAttribute(k_score_decode<kP256, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes) == cudaSuccess &&
+         cudaFuncSetAttribute(k_score_decode<kP256, kFused>, cudaFuncAttributePreferredSharedMemoryCarveout,
                               (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess;
 }
 
@@ -751,11 +773,11 @@ bool set_attrs() {
 int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, int64_t num_blocks, const int32_t* bt,
                     int64_t bt_stride, int32_t max_blocks, const int32_t* seq_lens, int32_t num_reqs,
                     int32_t query_len, int32_t width, float* scores, int32_t* status, cudaStream_t stream,
-                    int32_t page_tokens) {
+                    int32_t page_tokens, int32_t* fused_out, void* fused_ws, bool rank16) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IDX_E_CUDA;
   if (!g_attr[dev]) {
-    if (!set_attrs<false>() || !set_attrs<true>()) return IDX_E_CUDA;
+    if (!set_attrs<false, false>() || !set_attrs<true, false>() || !set_attrs<false, true>()) return IDX_E_CUDA;
     if (cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return IDX_E_CUDA;
     g_attr[dev] = true;
   }
@@ -764,10 +786,21 @@ int launch_score_tc(const uint8_t* q, const float* q_scale, const uint8_t* kv, i
   if (upper <= 0) return IDX_OK;
   if (upper > 0x7FFFFFFFLL) return IDX_E_TOO_LARGE;
   // one CTA per SM: each CTA holds all 512 TMEM columns of its SM
-  const int grid = (int)std::min<int64_t>((int64_t)g_sms[dev], upper);
-  launch_pdl(p256 ? k_score_decode<true> : k_score_decode<false>, dim3(grid), dim3(kThreads), kSmemBytes, stream, q,
-             q_scale, kv, num_blocks, bt, bt_stride, max_blocks, seq_lens, num_reqs, query_len, width, scores, status,
-             wait_polls());
+  int grid = (int)std::min<int64_t>((int64_t)g_sms[dev], upper);
+  fused::Args fa{};
+  if (fused_out) {
+    if (p256) return IDX_E_BAD_SHAPE;  // a slice may end between the two halves of a P256 page
+    grid = std::min(grid, fused::kMaxGrid);
+    fa.out = fused_out;
+    fa.counters = static_cast<uint32_t*>(fused_ws);
+    fa.cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(fused_ws) + fused::counter_bytes(num_reqs));
+    fa.rank16 = rank16;
+  }
+  void (*kernel)(const uint8_t*, const float*, const uint8_t*, int64_t, const int32_t*, int64_t, int32_t,
+                 const int32_t*, int32_t, int32_t, int32_t, float*, int32_t*, uint32_t, fused::Args) =
+      fused_out ? k_score_decode<false, true> : p256 ? k_score_decode<true, false> : k_score_decode<false, false>;
+  launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, q, q_scale, kv, num_blocks, bt, bt_stride,
+             max_blocks, seq_lens, num_reqs, query_len, width, scores, status, wait_polls(), fa);
   return launch_result();
 }
 

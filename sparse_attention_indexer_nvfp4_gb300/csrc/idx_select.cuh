@@ -188,7 +188,16 @@ __device__ __forceinline__ bool seg_slot(int i, int span) {
 // threshold is at or below the image of -inf (fewer than 16 lanes hold a
 // column above -inf), the images of every column are compared instead,
 // with 0 for "no column".
-template <int K, bool kForce, int kW>
+// Score loads: through the read-only path for rows written before the
+// kernel started, or from L2 (kCoherent) for rows written earlier in the
+// same kernel.
+template <bool kCoherent, typename T>
+__device__ __forceinline__ T ld_score(const T* p) {
+  if (kCoherent) return __ldcg(p);
+  return __ldg(p);
+}
+
+template <int K, bool kForce, int kW, bool kCoherent = false>
 __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
                                         bool rank16, bool pair) {
   static_assert(K % kW == 0, "16-byte loads fill kW elements at a time");
@@ -208,12 +217,12 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
     for (int j = 0; j < K / 4; ++j) {
       const int off = 128 * j + 4 * (int)lane;
       if (off + 3 < span) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(row + c0 + off));
+        const float4 v = ld_score<kCoherent>(reinterpret_cast<const float4*>(row + c0 + off));
         x[4 * j] = v.x, x[4 * j + 1] = v.y, x[4 * j + 2] = v.z, x[4 * j + 3] = v.w;
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (off + e < span) x[4 * j + e] = __ldg(row + c0 + off + e);
+          if (off + e < span) x[4 * j + e] = ld_score<kCoherent>(row + c0 + off + e);
       }
     }
   } else if (kW == 2) {
@@ -223,10 +232,10 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
     for (int j = 0; j < K / 2; ++j) {
       const int off = 64 * j + 2 * (int)lane;
       if (off + 1 < span) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(row2 + c0 + off));
+        const float4 v = ld_score<kCoherent>(reinterpret_cast<const float4*>(row2 + c0 + off));
         x[2 * j] = fmaxf(v.x, v.y), x[2 * j + 1] = fmaxf(v.z, v.w);
       } else if (off < span) {
-        const float2 h = __ldg(row2 + c0 + off);
+        const float2 h = ld_score<kCoherent>(row2 + c0 + off);
         x[2 * j] = fmaxf(h.x, h.y);
       }
     }
@@ -236,10 +245,10 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
       if (fixed(i) < lim) {
         const int col = c0 + i * 32 + (int)lane;
         if (pair) {
-          const float2 h = __ldg(reinterpret_cast<const float2*>(row) + col);
+          const float2 h = ld_score<kCoherent>(reinterpret_cast<const float2*>(row) + col);
           x[i] = fmaxf(h.x, h.y);
         } else {
-          x[i] = __ldg(row + col);
+          x[i] = ld_score<kCoherent>(row + col);
         }
       }
     }
@@ -323,15 +332,15 @@ __device__ uint64_t warp_top16_seg_impl(const float* __restrict__ row, int c0, i
 
 // Segments that start on a 16-byte boundary take 16-byte loads (four
 // scores, or two paired columns, per instruction); others one load per column.
-template <int K, bool kForce>
+template <int K, bool kForce, bool kCoherent = false>
 __device__ uint64_t warp_top16_seg(const float* __restrict__ row, int c0, int c1, int fb, int fe, WarpScratch* ws,
                                    bool rank16 = false, bool pair = false) {
   constexpr int kW4 = K % 4 == 0 ? 4 : 1, kW2 = K % 2 == 0 ? 2 : 1;
   if (!pair && (reinterpret_cast<uintptr_t>(row + c0) & 15u) == 0)
-    return warp_top16_seg_impl<K, kForce, kW4>(row, c0, c1, fb, fe, ws, rank16, pair);
+    return warp_top16_seg_impl<K, kForce, kW4, kCoherent>(row, c0, c1, fb, fe, ws, rank16, pair);
   if (pair && (reinterpret_cast<uintptr_t>(row + 2 * c0) & 15u) == 0)
-    return warp_top16_seg_impl<K, kForce, kW2>(row, c0, c1, fb, fe, ws, rank16, pair);
-  return warp_top16_seg_impl<K, kForce, 1>(row, c0, c1, fb, fe, ws, rank16, pair);
+    return warp_top16_seg_impl<K, kForce, kW2, kCoherent>(row, c0, c1, fb, fe, ws, rank16, pair);
+  return warp_top16_seg_impl<K, kForce, 1, kCoherent>(row, c0, c1, fb, fe, ws, rank16, pair);
 }
 
 }  // namespace sel

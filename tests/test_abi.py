@@ -68,7 +68,7 @@ def test_error_codes_and_strings(built):
     assert lib.idx_topk16_select(16, 100, 0, 100, None, 0, 0, None, None, None, 0, None) == 0
     assert lib.idx_mtp_score_fp8(16, 16, 4, 0, 16, 16, 8, 16, 4, 4, 16, 16, 2, 10, 16, None, None) == E_SHAPE
     assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 9000, 16, 16, None, 0, 0, None, None) == E_WS
-    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 4, None, None) == E_SHAPE  # flags
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 8, None, None) == E_SHAPE  # flags
 
 
 def test_wait_limit_setter_returns_the_previous_budget(built):
@@ -141,5 +141,20 @@ def test_decode_step_flags(built):
     E_SHAPE, E_MIS = -2, -3
     # P256 (flag 2) is accepted; with it the score buffer must be 8-byte aligned
     assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 20, 16, None, 0, 2, None, None) == E_MIS
-    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 4, None, None) == E_SHAPE
-    assert built.PAGE_256 == 2 and built.RANK_16BIT == 1
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 8, None, None) == E_SHAPE
+    assert built.PAGE_256 == 2 and built.RANK_16BIT == 1 and built.FUSED_SELECT == 4
+    # the fused step (flag 4): not with P256; its own zero-filled workspace
+    E_WS = -7
+    need = built.idx_decode_fused_workspace_bytes(1)
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, 4096, need, 6, None, None) == E_SHAPE
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, None, 0, 4, None, None) == E_WS
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, 4096, need - 8, 4, None, None) == E_WS
+    assert lib.idx_decode_step(16, 16, 16, 10, 16, 4, 4, 16, 1, 8, 40, 16, 16, 4100, need, 4, None, None) == E_MIS
+
+
+def test_fused_decode_workspace_sizing(built):
+    # counters (4 bytes a request, rounded up to 256), then (num_reqs + 512) x 32 rows x 16 keys of 8 bytes
+    for b in (1, 63, 64, 65, 20_000, 65_535):
+        assert built.idx_decode_fused_workspace_bytes(b) == -(-4 * b // 256) * 256 + (b + 512) * 32 * 16 * 8
+    assert built.idx_decode_fused_workspace_bytes(0) == 0
+    assert built.idx_decode_fused_workspace_bytes(65_536) == 0
