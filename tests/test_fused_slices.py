@@ -16,7 +16,11 @@ requests per slice, and confirm that
     below num_reqs + 512 (the workspace's slot count);
   * every request with pages is won by exactly one CTA, whose merge range
     holds exactly the CTAs that wrote its candidates;
-  * every request is written exactly once.
+  * every request is written exactly once;
+
+and that the merge of two descending candidate lists by rank counting is
+the top 16 of their union, so folding the parts' local top 16s gives the
+row's top 16.
 """
 
 import numpy as np
@@ -138,3 +142,45 @@ def test_slices_lists_slots_and_merges(case):
 
 def test_no_pages_at_all():
     simulate([0, 0, 0, 0], 152)
+
+
+def merge16(run, lst):
+    """Host restatement of the merge the fused step's last CTA uses: the top
+    16 of two descending lists of 16 distinct nonzero keys (0 padding); a
+    key's place is its index in its own list plus the larger keys of the
+    other list."""
+    top = [0] * 16
+    for own, other in ((run, lst), (lst, run)):
+        for idx, x in enumerate(own):
+            if x == 0:
+                continue
+            rank = idx + sum(1 for y in other if y > x)
+            if rank < 16:
+                top[rank] = x
+    return top
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_merge_of_sorted_lists_is_the_union_top16(seed):
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(2000):
+        keys = rng.choice(np.arange(1, 200, dtype=np.int64), size=int(rng.integers(0, 33)), replace=False)
+        split = int(rng.integers(0, len(keys) + 1))
+        a = sorted(keys[:split].tolist(), reverse=True)[:16]
+        b = sorted(keys[split:].tolist(), reverse=True)[:16]
+        pad = lambda v: v + [0] * (16 - len(v))
+        want = pad(sorted(a + b, reverse=True)[:16])
+        assert merge16(pad(a), pad(b)) == want
+    # folding the lists of several parts gives the top 16 of their union,
+    # which is the top 16 of the row when each part holds its own top 16
+    for _ in range(300):
+        row = rng.permutation(np.arange(1, 400, dtype=np.int64))[: int(rng.integers(1, 300))]
+        cuts = np.sort(rng.integers(0, len(row) + 1, size=int(rng.integers(0, 6))))
+        parts = np.split(row, cuts)
+        run = None
+        for p in parts:
+            loc = sorted(p.tolist(), reverse=True)[:16]
+            loc = loc + [0] * (16 - len(loc))
+            run = loc if run is None else merge16(run, loc)
+        want = sorted(row.tolist(), reverse=True)[:16]
+        assert run == want + [0] * (16 - len(want))
